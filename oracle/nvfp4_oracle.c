@@ -1,0 +1,552 @@
+/*
+ * NVFP4 oracle: a plain, slow, single-threaded CPU restatement of what the
+ * NVFP4 quantize + block-scaled matmul path computes.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library path links, loads or calls
+ * this file; it exists so the CUDA kernels can be checked against an
+ * independent implementation.  It shares no source with the CUDA code.
+ *
+ * Pages followed (cited by title and section):
+ *  [P1] "Entrenamiento de Modelos de Lenguaje con 4 Bits de Precisión"
+ *       (focoia.com.mx), sections "Características del Formato NVFP4" and
+ *       "Metodología de Entrenamiento", and the closing feature list.
+ *  [P2] "FP4 All the Way: Formación totalmente cuantificada de LLM"
+ *       (slashpage digest of Chmiel, Fishman, Banner, Soudry), section
+ *       "Describir" (the abstract).
+ *  [P3] "I ricercatori di Nvidia sbloccano il tutorial LLM ..."
+ *       (massacarraranews.com), section "Come funziona NVFP4?".
+ *
+ * What the pages fix: E2M1 elements with values ±0, ±0.5, ±1, ±1.5, ±2, ±3,
+ * ±4, ±6 [P1 "Características"], one E4M3 scale per 16 contiguous elements
+ * [P1 "Características"; P2 "Describir"], a multi-level scaling [P3 "Come
+ * funziona NVFP4?"], 2-D block scaling for weights, random Hadamard transforms
+ * and stochastic rounding of gradients [P1 "Metodología"], round-to-nearest in
+ * the forward pass and stochastic rounding in backward/update [P2 "Describir"].
+ * Everything the pages leave open is a stated reading (see the design notes);
+ * each is marked "reading" below.
+ *
+ * Floating point: every value that decides an integer (a scale byte, a code)
+ * is computed in IEEE binary32 with round-to-nearest-even, one operation at a
+ * time, in the order written here.  Build with -ffp-contract=off and without
+ * fast-math.  The matmul accumulates in binary64.
+ *
+ * Parity status per function:
+ *  - e2m1/e4m3 codecs, quantizers, RHT, swizzle, GEMM: pinned by the CPU tests
+ *    (tables from the pages, closed forms, invariants, brute force).
+ *  - philox4x32_10: the exact bit stream is "parity unpinned" (no published
+ *    known-answer values are used); its statistics are pinned.
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+#include <math.h>
+#include <float.h>
+
+#define OR_OK 0
+#define OR_ERR_NONFINITE 4
+#define OR_ERR_SHAPE 2
+
+/* ------------------------------------------------------------------------ */
+/* Element format: E2M1 [P1 "Características del Formato NVFP4"]            */
+/* ------------------------------------------------------------------------ */
+
+/* The eight magnitudes the page lists, indexed by the 3 low bits of a code.
+ * Reading: code bits are s e1 e0 m (sign = bit 3), exponent bias 1, so the
+ * magnitude codes 0..7 enumerate the listed values in increasing order. */
+static const float E2M1_MAG[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+
+float or_e2m1_value(int code)
+{
+    float m = E2M1_MAG[code & 7];
+    return (code & 8) ? -m : m;
+}
+
+/* Round-to-nearest onto the E2M1 grid [P2 "Describir": nearest rounding in
+ * the forward pass].  Reading: ties go to the code whose mantissa bit is 0
+ * (round-half-even), magnitudes above 6 saturate to 6, and the sign bit is
+ * kept even when the magnitude rounds to 0.  Written as a search for the
+ * nearest of the eight magnitudes. */
+int or_e2m1_rn(float v)
+{
+    int sign = signbit(v) ? 8 : 0;
+    double a = fabs((double)v);
+    if (a > 6.0)
+        return sign | 7;
+    int best = 0;
+    for (int c = 1; c < 8; ++c) {
+        double dc = fabs(a - (double)E2M1_MAG[c]);
+        double db = fabs(a - (double)E2M1_MAG[best]);
+        if (dc < db || (dc == db && (c & 1) == 0))
+            best = c;
+    }
+    return sign | best;
+}
+
+/* Stochastic rounding onto the E2M1 grid [P1 "Metodología": stochastic
+ * rounding on gradients; P2 "Describir": stochastic rounding in backward and
+ * update].  Reading: with lo/hi the neighbouring grid magnitudes around
+ * a = |v| and t = 256 (a - lo) / (hi - lo) (exact in binary32), the result is
+ * hi when (float)r + 0.5 < t for the random byte r, else lo.  |v| >= 6 gives 6.
+ * The sign is kept. */
+int or_e2m1_sr(float v, unsigned r)
+{
+    int sign = signbit(v) ? 8 : 0;
+    float a = fabsf(v);
+    if (!(a < 6.0f))
+        return sign | 7;
+    int lo = 0;
+    for (int c = 1; c < 8; ++c)
+        if (E2M1_MAG[c] <= a)
+            lo = c;
+    int hi = lo + 1;
+    float gap = E2M1_MAG[hi] - E2M1_MAG[lo];
+    float t = ((a - E2M1_MAG[lo]) / gap) * 256.0f;
+    float thr = (float)(r & 0xFFu) + 0.5f;
+    return sign | ((thr < t) ? hi : lo);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scale format: E4M3 [P1 "Características": one E4M3 factor per 16]        */
+/* ------------------------------------------------------------------------ */
+
+/* Reading: OCP E4M3 "FN" — 1 sign, 4 exponent (bias 7), 3 mantissa bits,
+ * subnormals at exponent 0, no infinities, S.1111.111 is NaN, largest finite
+ * value 448. */
+float or_e4m3_value(int code)
+{
+    int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    float v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexpf((float)m, -9);              /* m/8 * 2^(1-7) */
+    else
+        v = ldexpf((float)(8 + m), e - 10);    /* (1 + m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* Nearest finite E4M3 value with ties to the even code, for x >= 0 (the
+ * block scale is never negative).  Values beyond 448 (including +inf)
+ * saturate to 448; values at or below half the smallest subnormal round to 0.
+ * Written as a search over all 127 non-negative finite codes. */
+int or_e4m3_rn_sat(float x)
+{
+    double a = (double)x;
+    if (a != a)
+        return 0x7F;
+    if (a < 0)
+        a = 0; /* callers only pass non-negative values */
+    if (isinf(a))
+        return 0x7E;
+    int best = 0;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double dc = fabs(a - (double)or_e4m3_value(c));
+        double db = fabs(a - (double)or_e4m3_value(best));
+        if (dc < db || (dc == db && (c & 1) == 0))
+            best = c;
+    }
+    return best;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Counter-based generator: Philox4x32-10 (Salmon, Moraes, Dror, Shaw,      */
+/* "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11).  Ten rounds of    */
+/* the 4x32 Philox S-box with the Weyl key schedule, as that paper defines.  */
+/* ------------------------------------------------------------------------ */
+
+static void philox_round(uint32_t c[4], const uint32_t k[2])
+{
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ c[1] ^ k[0];
+    uint32_t n1 = lo1;
+    uint32_t n2 = hi0 ^ c[3] ^ k[1];
+    uint32_t n3 = lo0;
+    c[0] = n0; c[1] = n1; c[2] = n2; c[3] = n3;
+}
+
+void or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]};
+    uint32_t k[2] = {key[0], key[1]};
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k[0] += 0x9E3779B9u;
+            k[1] += 0xBB67AE85u;
+        }
+        philox_round(c, k);
+    }
+    memcpy(out, c, sizeof c);
+}
+
+/* Random byte for lane j of output block blk (reading): Philox with
+ * key = seed, counter = (blk lo, blk hi, 0, 0); byte j of the 128-bit result. */
+static unsigned sr_byte(uint64_t seed, uint64_t blk, int j)
+{
+    uint32_t ctr[4] = {(uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t w[4];
+    or_philox4x32_10(ctr, key, w);
+    return (w[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Random Hadamard transform [P1 "Metodología": random Hadamard transforms]  */
+/* ------------------------------------------------------------------------ */
+
+/* Sign diagonal (reading): bit i of word 0 of Philox(key = seed,
+ * counter = (0, 0, 1, 0)); a set bit flips lane i. */
+uint32_t or_rht_signs(uint64_t rht_seed)
+{
+    uint32_t ctr[4] = {0u, 0u, 1u, 0u};
+    uint32_t key[2] = {(uint32_t)rht_seed, (uint32_t)(rht_seed >> 32)};
+    uint32_t w[4];
+    or_philox4x32_10(ctr, key, w);
+    return w[0] & 0xFFFFu;
+}
+
+/* y = (1/4) H16 D v with H16 the Sylvester Hadamard matrix of order 16.
+ * Reading of the arithmetic: flip signs (exact), then the fast Walsh-Hadamard
+ * butterflies with strides 1, 2, 4, 8 in that order, each pair (a, b) ->
+ * (a + b, a - b) rounded to binary32, then multiply by 0.25. */
+void or_rht16(const float v[16], uint32_t sign_bits, float y[16])
+{
+    float u[16];
+    for (int i = 0; i < 16; ++i)
+        u[i] = ((sign_bits >> i) & 1u) ? -v[i] : v[i];
+    for (int h = 1; h < 16; h *= 2) {
+        for (int i = 0; i < 16; ++i) {
+            if (i & h)
+                continue;
+            float a = u[i], b = u[i + h];
+            u[i] = a + b;
+            u[i + h] = a - b;
+        }
+    }
+    for (int i = 0; i < 16; ++i)
+        y[i] = u[i] * 0.25f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scale-factor layout (reading): 128-row x 4-block atoms of 512 bytes, the  */
+/* layout block-scaled tensor-core matmuls read scale factors in.            */
+/* ------------------------------------------------------------------------ */
+
+int64_t or_sf_groups(int64_t kblocks) { return (kblocks + 3) / 4; }
+
+size_t or_sf_bytes(int64_t rows, int64_t cols)
+{
+    int64_t rt = (rows + 127) / 128;
+    return (size_t)(rt * or_sf_groups(cols / 16) * 512);
+}
+
+size_t or_sf_offset(int64_t r, int64_t kb, int64_t kblocks)
+{
+    int64_t cp = or_sf_groups(kblocks);
+    return (size_t)(((r / 128) * cp + kb / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (kb % 4));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantizers                                                               */
+/* ------------------------------------------------------------------------ */
+
+static float bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* Second (tensor) level of the multi-level scaling [P3 "Come funziona
+ * NVFP4?"]; binary32 per-tensor scale (reading): s_enc = 2688 / amax with
+ * 2688 = 6 * 448 (largest E2M1 times largest E4M3), saturated to FLT_MAX; the
+ * stored decode scale is g = amax / 2688.  amax == 0 gives g = 0. */
+static void tensor_scales(float amax, float* s_enc, float* g)
+{
+    if (amax == 0.0f) {
+        *s_enc = 0.0f;
+        *g = 0.0f;
+        return;
+    }
+    float s = 2688.0f / amax;
+    if (isinf(s))
+        s = FLT_MAX;
+    *s_enc = s;
+    *g = amax / 2688.0f;
+}
+
+/* First (block) level: the E4M3 scale of a block with maximum magnitude
+ * bamax [P1 "Características"; P2 "Describir"].  Reading:
+ * sb = e4m3(rn(rn(bamax / 6) * s_enc)). */
+static int block_scale(float bamax, float s_enc)
+{
+    float t = bamax / 6.0f;
+    float sbf = t * s_enc;
+    return or_e4m3_rn_sat(sbf);
+}
+
+/* Quantize the 16 values of one block with scale byte sb (reading):
+ * f = rn(s_enc / dec(sb)); v = rn(x * f) (zero stays signed zero; dec(sb) == 0
+ * sends every element to signed zero); then RN or SR onto E2M1. */
+static void quantize_block(const float x[16], float s_enc, int sb, int mode,
+                           uint64_t seed, uint64_t blk, int codes[16])
+{
+    float d = or_e4m3_value(sb);
+    float f = (d == 0.0f) ? 0.0f : s_enc / d;
+    for (int j = 0; j < 16; ++j) {
+        float v;
+        if (d == 0.0f || x[j] == 0.0f)
+            v = signbit(x[j]) ? -0.0f : 0.0f;
+        else
+            v = x[j] * f;
+        codes[j] = (mode == 1) ? or_e2m1_sr(v, sr_byte(seed, blk, j)) : or_e2m1_rn(v);
+    }
+}
+
+static void put_code(uint8_t* q, int64_t row_bytes, int64_t r, int64_t c, int code)
+{
+    uint8_t* p = q + r * row_bytes + c / 2;
+    if (c & 1)
+        *p = (uint8_t)((*p & 0x0F) | (code << 4));
+    else
+        *p = (uint8_t)((*p & 0xF0) | code);
+}
+
+/* 1x16 quantization along rows (the contiguous axis) [P1 "Características":
+ * each block of 16 contiguous elements shares an E4M3 scale].
+ * x: bf16 bits, R x C with leading dimension ld.  Outputs: q (R x C/2 bytes,
+ * element 2i in the low nibble), sf (swizzled, padding zero), *g.
+ * mode 0 = round-to-nearest, 1 = stochastic (random byte per element). */
+int or_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int mode, uint64_t seed,
+                uint8_t* q, uint8_t* sf, float* g)
+{
+    if (C % 16 != 0 || R < 0 || C < 0)
+        return OR_ERR_SHAPE;
+    const int64_t KB = C / 16;
+    float amax = 0.0f;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            float a = fabsf(bf16_to_f32(x[r * ld + c]));
+            if (!(a <= FLT_MAX))
+                return OR_ERR_NONFINITE;
+            if (a > amax)
+                amax = a;
+        }
+    float s_enc, gd;
+    tensor_scales(amax, &s_enc, &gd);
+    *g = gd;
+    memset(sf, 0, or_sf_bytes(R, C));
+    memset(q, 0, (size_t)(R * (C / 2)));
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            float xb[16];
+            float bamax = 0.0f;
+            for (int j = 0; j < 16; ++j) {
+                xb[j] = bf16_to_f32(x[r * ld + kb * 16 + j]);
+                if (fabsf(xb[j]) > bamax)
+                    bamax = fabsf(xb[j]);
+            }
+            int sb = (amax == 0.0f) ? 0 : block_scale(bamax, s_enc);
+            int codes[16];
+            quantize_block(xb, s_enc, sb, mode, seed, (uint64_t)(r * KB + kb), codes);
+            for (int j = 0; j < 16; ++j)
+                put_code(q, C / 2, r, kb * 16 + j, codes[j]);
+            sf[or_sf_offset(r, kb, KB)] = (uint8_t)sb;
+        }
+    return OR_OK;
+}
+
+/* 2-D block scaling for weights [P1 "Metodología": two-dimensional block
+ * scaling for weights]; 16 x 16 tiles (reading).  One scale per tile, from the
+ * tile's maximum magnitude, stored in every row's entry; elements are rounded
+ * to nearest.  Optional transposed outputs: qT (C x R/2) is the exact
+ * transpose of the codes and sfT gives tile (i, j)'s scale to tile (j, i). */
+int or_quantize_2d(const uint16_t* w, int64_t R, int64_t C, int64_t ld,
+                   uint8_t* q, uint8_t* sf, uint8_t* qT, uint8_t* sfT, float* g)
+{
+    if (C % 16 != 0 || R % 16 != 0 || R < 0 || C < 0)
+        return OR_ERR_SHAPE;
+    const int64_t KB = C / 16, KBT = R / 16;
+    float amax = 0.0f;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            float a = fabsf(bf16_to_f32(w[r * ld + c]));
+            if (!(a <= FLT_MAX))
+                return OR_ERR_NONFINITE;
+            if (a > amax)
+                amax = a;
+        }
+    float s_enc, gd;
+    tensor_scales(amax, &s_enc, &gd);
+    *g = gd;
+    memset(sf, 0, or_sf_bytes(R, C));
+    memset(q, 0, (size_t)(R * (C / 2)));
+    if (qT) memset(qT, 0, (size_t)(C * (R / 2)));
+    if (sfT) memset(sfT, 0, or_sf_bytes(C, R));
+    for (int64_t tr = 0; tr < R / 16; ++tr)
+        for (int64_t tc = 0; tc < KB; ++tc) {
+            float bamax = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                for (int j = 0; j < 16; ++j) {
+                    float a = fabsf(bf16_to_f32(w[(tr * 16 + i) * ld + tc * 16 + j]));
+                    if (a > bamax)
+                        bamax = a;
+                }
+            int sb = (amax == 0.0f) ? 0 : block_scale(bamax, s_enc);
+            for (int i = 0; i < 16; ++i) {
+                int64_t r = tr * 16 + i;
+                float xb[16];
+                for (int j = 0; j < 16; ++j)
+                    xb[j] = bf16_to_f32(w[r * ld + tc * 16 + j]);
+                int codes[16];
+                quantize_block(xb, s_enc, sb, 0, 0, 0, codes);
+                for (int j = 0; j < 16; ++j) {
+                    put_code(q, C / 2, r, tc * 16 + j, codes[j]);
+                    if (qT)
+                        put_code(qT, R / 2, tc * 16 + j, r, codes[j]);
+                }
+                sf[or_sf_offset(r, tc, KB)] = (uint8_t)sb;
+            }
+            if (sfT)
+                for (int j = 0; j < 16; ++j)
+                    sfT[or_sf_offset(tc * 16 + j, tr, KBT)] = (uint8_t)sb;
+        }
+    return OR_OK;
+}
+
+/* Wgrad operand: random Hadamard transform along the token axis, then 1x16
+ * quantization along that axis, written transposed [P1 "Metodología": random
+ * Hadamard transforms, stochastic rounding on gradients].  Reading: for each
+ * channel c and each 16-token chunk, y = (1/4) H16 D v with the seeded sign
+ * diagonal D (the same for every chunk); the tensor scale uses the maximum
+ * magnitude of the transformed values; the transformed binary32 values are
+ * quantized as they are.  Output qT is C x T/2 (channel-major, tokens
+ * contiguous), sfT is swizzled with C rows and T/16 blocks; the SR counter is
+ * the block index in that output layout. */
+int or_rht_quantize(const uint16_t* x, int64_t T, int64_t C, int64_t ld, uint64_t rht_seed,
+                    int mode, uint64_t sr_seed, uint8_t* qT, uint8_t* sfT, float* g)
+{
+    if (T % 16 != 0 || T < 0 || C < 0)
+        return OR_ERR_SHAPE;
+    const int64_t KB = T / 16;
+    const uint32_t signs = or_rht_signs(rht_seed);
+    float amax = 0.0f;
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            float v[16], y[16];
+            for (int i = 0; i < 16; ++i)
+                v[i] = bf16_to_f32(x[(kb * 16 + i) * ld + c]);
+            or_rht16(v, signs, y);
+            for (int i = 0; i < 16; ++i) {
+                float a = fabsf(y[i]);
+                if (!(a <= FLT_MAX))
+                    return OR_ERR_NONFINITE;
+                if (a > amax)
+                    amax = a;
+            }
+        }
+    float s_enc, gd;
+    tensor_scales(amax, &s_enc, &gd);
+    *g = gd;
+    memset(sfT, 0, or_sf_bytes(C, T));
+    memset(qT, 0, (size_t)(C * (T / 2)));
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            float v[16], y[16];
+            for (int i = 0; i < 16; ++i)
+                v[i] = bf16_to_f32(x[(kb * 16 + i) * ld + c]);
+            or_rht16(v, signs, y);
+            float bamax = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                if (fabsf(y[i]) > bamax)
+                    bamax = fabsf(y[i]);
+            int sb = (amax == 0.0f) ? 0 : block_scale(bamax, s_enc);
+            int codes[16];
+            quantize_block(y, s_enc, sb, mode, sr_seed, (uint64_t)(c * KB + kb), codes);
+            for (int i = 0; i < 16; ++i)
+                put_code(qT, T / 2, c, kb * 16 + i, codes[i]);
+            sfT[or_sf_offset(c, kb, KB)] = (uint8_t)sb;
+        }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantization and the block-scaled matmul [P1: NVFP4 runs on Blackwell  */
+/* tensor cores]: value = e2m1(code) * e4m3(block scale) * g.               */
+/* ------------------------------------------------------------------------ */
+
+static double deq(const uint8_t* q, const uint8_t* sf, int64_t r, int64_t c, int64_t C)
+{
+    uint8_t byte = q[r * (C / 2) + c / 2];
+    int code = (c & 1) ? (byte >> 4) : (byte & 15);
+    double s = (double)or_e4m3_value(sf[or_sf_offset(r, c / 16, C / 16)]);
+    return (double)or_e2m1_value(code) * s;
+}
+
+void or_dequantize(const uint8_t* q, const uint8_t* sf, float g, int64_t R, int64_t C, double* out)
+{
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c)
+            out[r * C + c] = deq(q, sf, r, c, C) * (double)g;
+}
+
+/* D[m][n] = gA gB sum_k deqA[m][k] deqB[n][k] with A (M x K) and B (N x K)
+ * both stored K-contiguous; accumulated in binary64.  dabs receives
+ * gA gB sum_k |deqA deqB| (for error bounds).  Either output may be NULL. */
+void or_gemm_f64(const uint8_t* a, const uint8_t* sfa, float ga, const uint8_t* b,
+                 const uint8_t* sfb, float gb, int64_t M, int64_t N, int64_t K,
+                 double* d, double* dabs)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double s = 0.0, sa = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = deq(a, sfa, m, k, K) * deq(b, sfb, n, k, K);
+                s += p;
+                sa += fabs(p);
+            }
+            if (d) d[m * N + n] = (double)ga * (double)gb * s;
+            if (dabs) dabs[m * N + n] = (double)ga * (double)gb * sa;
+        }
+}
+
+/* The same matmul evaluated only at the listed (m, n) pairs. */
+void or_gemm_f64_sampled(const uint8_t* a, const uint8_t* sfa, float ga, const uint8_t* b,
+                         const uint8_t* sfb, float gb, int64_t M, int64_t N, int64_t K,
+                         const int64_t* ms, const int64_t* ns, int64_t count,
+                         double* d, double* dabs)
+{
+    (void)M; (void)N;
+    for (int64_t i = 0; i < count; ++i) {
+        double s = 0.0, sa = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = deq(a, sfa, ms[i], k, K) * deq(b, sfb, ns[i], k, K);
+            s += p;
+            sa += fabs(p);
+        }
+        d[i] = (double)ga * (double)gb * s;
+        dabs[i] = (double)ga * (double)gb * sa;
+    }
+}
+
+/* Batch helpers so tests can sweep the element codecs without a Python loop. */
+void or_e2m1_rn_many(const float* v, int64_t n, uint8_t* out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (uint8_t)or_e2m1_rn(v[i]);
+}
+
+void or_e2m1_sr_many(const float* v, const uint8_t* r, int64_t n, uint8_t* out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (uint8_t)or_e2m1_sr(v[i], r[i]);
+}
+
+void or_e4m3_rn_sat_many(const float* v, int64_t n, uint8_t* out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (uint8_t)or_e4m3_rn_sat(v[i]);
+}
