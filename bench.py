@@ -1,0 +1,483 @@
+#!/usr/bin/env python
+"""NVFP4 linear-layer benchmark on one GB300 (or N independent replicas).
+
+One step = the whole NVFP4 hot path of a 7B-shape MLP (hidden 4096, FFN 11008,
+8192 tokens, no activation function) forward and backward, 16 kernel launches:
+
+  quantize(X, RN) . quantize_2d(W_up, +T) . GEMM  H  = X W_up^T
+  quantize(H, RN) . quantize_2d(W_down, +T) . GEMM  Y  = H W_down^T
+  quantize(dY, SR) . GEMM dH = dY W_down                     (Dgrad down)
+  rht_quantize(dY, SR) . rht_quantize(H, RN) . GEMM dW_down = dY^T H (Wgrad)
+  quantize(dH, SR) . GEMM dX = dH W_up                       (Dgrad up)
+  rht_quantize(dH, SR) . rht_quantize(X, RN) . GEMM dW_up = dH^T X  (Wgrad)
+
+Six GEMMs of 2*8192*11008*4096 flops.  `value` is NVFP4 TFLOP/s of the whole
+step (all quantizers included) with inputs resident in HBM; `e2e` is the same
+metric with the inputs copied from pinned host memory and the step's outputs
+(Y, dX, dW_up, dW_down) copied back inside the timed region.  The inputs of a
+step (~0.8 GB touched) exceed the 129 MB L2, so no flush is needed.
+
+--impl reference times the CPU oracle (the plain C restatement) on a bounded
+sample of the same workload and reports the same metric, extrapolated.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "mlp7b_fwd_bwd_h4096_f11008_t8192"
+TOKENS, HIDDEN, FFN = 8192, 4096, 11008
+GEMM_FLOPS = 2.0 * TOKENS * HIDDEN * FFN
+N_GEMMS = 6
+METRIC = "NVFP4 GEMM TFLOPS & quantize GB/s at 1 GB300, as fraction of roofline"
+L2_BYTES = 129e6
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio (fp4 13.5 PF, bf16 2.25 PF)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        p = json.load(open(path))
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def quant_bytes(kind: str, rows: int, cols: int) -> float:
+    """Algorithmic HBM bytes of one quantizer launch: bf16 read once (twice when
+    the tensor exceeds half the L2, since the tensor amax must be known before
+    any code is written), plus packed codes and scale bytes written."""
+    n = rows * cols
+    reads = 1 if 2 * n <= 0.5 * L2_BYTES else 2
+    out = n / 2 + n / 16
+    if kind == "quantize_2d_t":
+        out *= 2
+    return reads * 2.0 * n + out
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["nvfp4_bit_quantized_quantize_gb300/csrc/gemm.cu", "nvfp4_bit_quantized_quantize_gb300/csrc/device.cuh"]
+
+
+def traffic_for(kernel: str, src_hash: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current source of that kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        t = json.load(open(path))[kernel]
+        if t.get("source_hash") == src_hash:
+            return float(t["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ clocks ----
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"nvfp4_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower().startswith("active")})
+        sm = [r[0] for r in rows]
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": reasons}
+
+
+# --------------------------------------------------------------- our arm ----
+
+class MlpStep:
+    """Device buffers and the 16 launches of one fwd+bwd step."""
+
+    def __init__(self, dev):
+        import numpy as np
+        import torch
+
+        import nvfp4_bit_quantized_quantize_gb300 as nv
+        from nvfp4_bit_quantized_quantize_gb300 import synth
+
+        self.nv, self.torch = nv, torch
+        self.dev = dev
+        host = synth.make_workload(WORKLOAD)
+        self.seed = synth.WORKLOADS[WORKLOAD]["seed"]
+        bf = torch.bfloat16
+        # pinned host copies (for the end-to-end leg) and device inputs
+        self.h_in = {k: torch.from_numpy(v.view(np.int16)).view(bf).pin_memory() for k, v in host.items()}
+        self.d_in = {k: v.to(dev, non_blocking=False) for k, v in self.h_in.items()}
+        T, D, F = TOKENS, HIDDEN, FFN
+        e = lambda *s: torch.empty(s, dtype=bf, device=dev)
+        self.H, self.Y, self.dH, self.dX = e(T, F), e(T, D), e(T, F), e(T, D)
+        self.dW_up, self.dW_down = e(F, D), e(D, F)
+        self.h_out = {k: torch.empty(v.shape, dtype=bf).pin_memory()
+                      for k, v in {"Y": self.Y, "dX": self.dX, "dW_up": self.dW_up, "dW_down": self.dW_down}.items()}
+        q = lambda r, c: nv.alloc_quantized(r, c, dev)
+        self.xq, self.wuq, self.wuqT = q(T, D), q(F, D), q(D, F)
+        self.hq, self.wdq, self.wdqT = q(T, F), q(D, F), q(F, D)
+        self.dyq, self.dyT, self.hT = q(T, D), q(D, T), q(F, T)
+        self.dhq, self.dhT, self.xT = q(T, F), q(F, T), q(D, T)
+        self.ws = nv.alloc_workspace(dev)
+        torch.cuda.synchronize(dev)
+
+    def launches(self):
+        nv = self.nv
+        x, wu, wd, dy = self.d_in["X"], self.d_in["W_up"], self.d_in["W_down"], self.d_in["dY_down"]
+        T, D, F = TOKENS, HIDDEN, FFN
+        ws, s = self.ws, self.seed
+        rht_seed = s + 1
+        Q = nv.nvfp4_quantize
+        Q2 = nv.nvfp4_quantize_2d
+        R = nv.nvfp4_rht_quantize
+
+        def G(a, b, d, M, N, K):
+            return lambda: nv.nvfp4_gemm(a[0], a[1], a[2], b[0], b[1], b[2], M, N, K, d, N, nv.OUT_BF16, ws)
+
+        return [
+            ("quantize_1x16", ("rn", T, D), lambda: Q(x, T, D, D, nv.RN, 0, *self.xq, ws)),
+            ("quantize_2d_t", ("rn", F, D), lambda: Q2(wu, F, D, D, self.wuq[0], self.wuq[1], self.wuqT[0],
+                                                       self.wuqT[1], self.wuq[2], ws)),
+            ("gemm", (T, F, D), G(self.xq, self.wuq, self.H, T, F, D)),
+            ("quantize_1x16", ("rn", T, F), lambda: Q(self.H, T, F, F, nv.RN, 0, *self.hq, ws)),
+            ("quantize_2d_t", ("rn", D, F), lambda: Q2(wd, D, F, F, self.wdq[0], self.wdq[1], self.wdqT[0],
+                                                       self.wdqT[1], self.wdq[2], ws)),
+            ("gemm", (T, D, F), G(self.hq, self.wdq, self.Y, T, D, F)),
+            ("quantize_1x16", ("sr", T, D), lambda: Q(dy, T, D, D, nv.SR, s * 16 + 3, *self.dyq, ws)),
+            ("gemm", (T, F, D), G(self.dyq, (self.wdqT[0], self.wdqT[1], self.wdq[2]), self.dH, T, F, D)),
+            ("rht_quantize", ("sr", T, D), lambda: R(dy, T, D, D, rht_seed, nv.SR, s * 16 + 4, *self.dyT, ws)),
+            ("rht_quantize", ("rn", T, F), lambda: R(self.H, T, F, F, rht_seed, nv.RN, 0, *self.hT, ws)),
+            ("gemm", (D, F, T), G(self.dyT, self.hT, self.dW_down, D, F, T)),
+            ("quantize_1x16", ("sr", T, F), lambda: Q(self.dH, T, F, F, nv.SR, s * 16 + 5, *self.dhq, ws)),
+            ("gemm", (T, D, F), G(self.dhq, (self.wuqT[0], self.wuqT[1], self.wuq[2]), self.dX, T, D, F)),
+            ("rht_quantize", ("sr", T, F), lambda: R(self.dH, T, F, F, rht_seed, nv.SR, s * 16 + 6, *self.dhT, ws)),
+            ("rht_quantize", ("rn", T, D), lambda: R(x, T, D, D, rht_seed, nv.RN, 0, *self.xT, ws)),
+            ("gemm", (F, D, T), G(self.dhT, self.xT, self.dW_up, F, D, T)),
+        ]
+
+    def h2d(self):
+        for k, v in self.h_in.items():
+            self.d_in[k].copy_(v, non_blocking=True)
+        return sum(v.numel() * 2 for v in self.h_in.values())
+
+    def d2h(self):
+        src = {"Y": self.Y, "dX": self.dX, "dW_up": self.dW_up, "dW_down": self.dW_down}
+        for k, v in src.items():
+            self.h_out[k].copy_(v, non_blocking=True)
+        return sum(v.numel() * 2 for v in src.values())
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from __graft_entry__ import build
+    build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    step = MlpStep(dev)
+    launches = step.launches()
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        for _, _, fn in launches:
+            fn()
+    st = step.nv.nvfp4_device_status(step.ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {step.nv.nvfp4_status_str(st)}")
+    barrier()
+
+    # ---- timed region: inputs resident in HBM; one event pair per launch ----
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in launches]
+           for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t0.record(stream)
+    for k in range(args.steps):
+        for (_, _, fn), (a, b) in zip(launches, evs[k]):
+            a.record(stream)
+            fn()
+            b.record(stream)
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    st = step.nv.nvfp4_device_status(step.ws)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {step.nv.nvfp4_status_str(st)}")
+
+    per_kind = {}
+    for k in range(args.steps):
+        for (kind, shape, _), (a, b) in zip(launches, evs[k]):
+            per_kind.setdefault((kind, shape), []).append(a.elapsed_time(b))
+    ms_step = ms_total / args.steps
+    flops_step = N_GEMMS * GEMM_FLOPS
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    pk = peaks()
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    gemm_ms = [t for (kind, _), ts in per_kind.items() if kind == "gemm" for t in ts]
+    gemm_avg = statistics.mean(gemm_ms)
+    gemm_tflops = GEMM_FLOPS / (gemm_avg * 1e-3) / 1e12
+    kernels = {}
+    for (kind, shape), ts in per_kind.items():
+        avg = statistics.mean(ts)
+        key = f"{kind}[{'x'.join(str(s) for s in shape)}]"
+        if kind == "gemm":
+            f = 2.0 * shape[0] * shape[1] * shape[2]
+            kernels[key] = {"ms": round(avg, 4), "TFLOP/s": round(f / (avg * 1e-3) / 1e12, 1),
+                            "frac": round(f / (avg * 1e-3) / 1e12 / fp4_peak, 3)}
+        else:
+            byts = quant_bytes(kind, shape[1], shape[2])
+            gbs = byts / (avg * 1e-3) / 1e9
+            kernels[key] = {"ms": round(avg, 4), "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 3)}
+    q_ms = sum(statistics.mean(ts) for (kind, _), ts in per_kind.items() if kind != "gemm")
+    q_bytes = sum(quant_bytes(kind, sh[1], sh[2]) * len(ts) / args.steps
+                  for (kind, sh), ts in per_kind.items() if kind != "gemm")
+    step_kernel_ms = sum(statistics.mean(ts) * len(ts) / args.steps for ts in per_kind.values())
+
+    src_hash = source_hash(GEMM_SOURCES)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 codes, e4m3 block scales, f32 tensor scale) -> f32 accumulate -> bf16",
+        "data": "synthetic (seeded N(0,1)/N(0,0.02)/N(0,1e-3), 0.1% outliers x100 on X)",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
+                   "gemms_per_step": N_GEMMS, "launches_per_step": len(launches),
+                   "l2": "inputs larger than L2 (about 0.8 GB touched per step), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "nvf4_gemm_kernel", "achieved": round(gemm_tflops, 1),
+                     "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak, 4),
+                     "traffic": traffic_for("nvf4_gemm_kernel", src_hash),
+                     "peak_note": f"{pk['source']} bf16 burst {pk['bf16_tflops']} x {FP4_OVER_BF16} (fp4/bf16 nominal)",
+                     "algorithmic_flops_per_launch": GEMM_FLOPS},
+        "quantize": {"GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
+                     "frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+                     "peak_gbs": pk["hbm_gbs"], "ms_per_step": round(q_ms, 4)},
+        "kernels": kernels,
+        "kernel_ms_per_step": round(step_kernel_ms, 4),
+        "gpu_launches": len(launches) * args.steps,
+        "clocks": clk,
+    }
+
+    # ---- end to end: pinned host inputs in, results out, every step ----
+    if not args.no_e2e:
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h2d = d2h = 0
+        for k in range(args.steps):
+            h2d = step.h2d()
+            for _, _, fn in launches:
+                fn()
+            d2h = step.d2h()
+        e1.record(stream)
+        barrier()
+        ms_e2e = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms_e2e = float(tt.item())
+        line["e2e"] = {"value": round(world * flops_step / (ms_e2e / args.steps * 1e-3) / 1e12, 2),
+                       "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(ms_e2e / args.steps, 4)}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    return line
+
+
+# ------------------------------------------------------- CPU oracle arm ----
+
+def oracle_step_estimate(budget_s: float):
+    """Time the oracle on bounded samples of every kind of launch of the step
+    (each sample sized to about a fifth of budget_s) and extrapolate the time of
+    one full step.  Returns (seconds, sample description)."""
+    import numpy as np
+
+    import oracle as O
+    from nvfp4_bit_quantized_quantize_gb300 import synth
+
+    T, D, F = TOKENS, HIDDEN, FFN
+    share = budget_s / 5.0
+
+    def per_unit(make, run, units, lo=1):
+        """Grow the sample until one run takes about `share` seconds."""
+        n = lo
+        while True:
+            arg = make(n)
+            t = time.perf_counter()
+            run(arg)
+            dt = time.perf_counter() - t
+            if dt >= share * 0.5 or n >= (1 << 20):
+                return dt / units(n), n
+            n = max(n * 2, int(n * share / max(dt, 1e-4) * 0.9))
+
+    rng = np.random.default_rng(0)
+    mk_x = lambda r: synth.normal_bf16((r, D), 4, 0, 1.0, 0.0, 0.001, 100.0)
+    t_rn, r_rn = per_unit(mk_x, lambda x: O.quantize(x, O.RN), lambda r: r * D, 16)
+    t_sr, r_sr = per_unit(mk_x, lambda x: O.quantize(x, O.SR, 1), lambda r: r * D, 16)
+    t_2d, r_2d = per_unit(lambda r: synth.normal_bf16((16 * r, D), 4, 1, 0.02), O.quantize_2d,
+                          lambda r: 16 * r * D, 1)
+    t_rht, c_rht = per_unit(lambda c: synth.normal_bf16((T, 8 * c), 4, 2, 1e-3),
+                            lambda x: O.rht_quantize(x, 5, O.SR, 1), lambda c: T * 8 * c, 1)
+    K = D
+    qa = rng.integers(0, 256, (64, K // 2), dtype=np.uint8)
+    sa = np.full(O.sf_bytes(64, K), 0x38, np.uint8)
+    t_mac, n_out = per_unit(lambda n: (np.arange(n) % 64, (np.arange(n) * 7) % 64),
+                            lambda mn: O.gemm_f64_sampled(qa, sa, 1.0, qa, sa, 1.0, 64, 64, K, mn[0], mn[1]),
+                            lambda n: n * K, 8)
+
+    el = lambda r, c: r * c
+    quant = (t_rn * (el(T, D) + el(T, F)) + t_sr * (el(T, D) + el(T, F)) + t_2d * (el(F, D) + el(D, F))
+             + t_rht * (el(T, D) * 2 + el(T, F) * 2))
+    total = quant + t_mac * (N_GEMMS * GEMM_FLOPS / 2)
+    sample = (f"oracle timed on {r_rn}x{D} (1x16 RN), {r_sr}x{D} (1x16 SR), {16 * r_2d}x{D} (2-D), "
+              f"{T}x{8 * c_rht} (RHT+SR) slices and {n_out} GEMM outputs at K={K}; per-element and "
+              f"per-MAC times extrapolated to the full step ({N_GEMMS} GEMMs, 10 quantizer launches)")
+    return total, sample
+
+
+def cpu_baseline(budget_s: float = 15.0):
+    t = time.perf_counter()
+    est, sample = oracle_step_estimate(budget_s)
+    wall = time.perf_counter() - t
+    return {"value": N_GEMMS * GEMM_FLOPS / est / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": sample + f" (measured in {wall:.1f} s, single thread)",
+            "extrapolated_step_s": round(est, 1)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    ests = []
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        est, sample = oracle_step_estimate(budget_s=args.cpu_budget / 3)
+        if i >= args.warmup:
+            ests.append(est)
+    s_step = statistics.median(ests)
+    value = N_GEMMS * GEMM_FLOPS / s_step / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 decisions, f64 GEMM accumulation (oracle)",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

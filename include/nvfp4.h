@@ -1,0 +1,181 @@
+/*
+ * nvfp4.h — C ABI of the GB300 (sm_103a) NVFP4 quantize + block-scaled GEMM
+ * library (libnvfp4_gb300.so).
+ *
+ * The format, as the pages define it:
+ *  - every element is E2M1 (1 sign, 2 exponent, 1 mantissa bit), one of
+ *    ±0, ±0.5, ±1, ±1.5, ±2, ±3, ±4, ±6
+ *    ["Entrenamiento de Modelos de Lenguaje con 4 Bits de Precisión",
+ *     section "Características del Formato NVFP4"];
+ *  - each block of 16 contiguous elements shares one E4M3 scale
+ *    [same section; "FP4 All the Way: Formación totalmente cuantificada de
+ *     LLM", section "Describir"];
+ *  - scaling is multi-level ["I ricercatori di Nvidia sbloccano ...",
+ *    section "Come funziona NVFP4?"]: here a binary32 tensor scale over the
+ *    block scales;
+ *  - the training recipe adds 2-D block scaling for weights, random Hadamard
+ *    transforms and stochastic rounding of gradients ["Entrenamiento ...",
+ *    section "Metodología de Entrenamiento"]; round-to-nearest in the
+ *    forward pass, stochastic rounding in backward and update ["FP4 All the
+ *    Way", section "Describir"].
+ *
+ * Arithmetic (readings where the pages are silent):
+ *  - amax = max |x| over the tensor (over the transformed values for the
+ *    Hadamard variant); s_enc = 2688 / amax (binary32, saturated to FLT_MAX),
+ *    g = amax / 2688 is the stored decode scale (0 when amax == 0);
+ *  - block scale byte = E4M3(rn(rn(bamax / 6) * s_enc)), nearest-even,
+ *    saturating at 448;
+ *  - f = rn(s_enc / E4M3value(byte)); v = rn(x * f); E2M1 code by nearest-even
+ *    (NVFP4_ROUND_RN) or stochastic rounding (NVFP4_ROUND_SR) with one random
+ *    byte per element from Philox4x32-10 (key = seed, counter = (block index,
+ *    0, 0)); |v| above 6 saturates; the sign bit is kept;
+ *  - decoded value of element (r, c) = E2M1(code) * E4M3(scale(r, c/16)) * g.
+ *
+ * Layouts:
+ *  - bf16 inputs are row-major with a leading dimension `ld` in elements;
+ *  - codes are packed two per byte, element 2i in the low nibble, rows dense
+ *    (row stride = cols / 2 bytes);
+ *  - scale bytes use the 128 x 4 atom layout block-scaled tensor-core matmuls
+ *    read: byte of (row r, block kb) at
+ *      ((r / 128) * Cp + kb / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + kb % 4,
+ *    Cp = ceil(kblocks / 4); rows are padded to 128 and blocks to 4, padding
+ *    is written as 0 by the quantizers.  Size: nvfp4_sf_bytes(rows, cols).
+ *
+ * Conventions for every call:
+ *  - all data pointers are DEVICE pointers owned by the caller; the library
+ *    allocates nothing and keeps no state between calls;
+ *  - calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream); argument, shape and alignment errors are returned
+ *    before anything is launched;
+ *  - `ws` is a caller-owned device workspace of nvfp4_workspace_bytes()
+ *    bytes, zeroed once with nvfp4_workspace_init before first use; every
+ *    call leaves it ready for the next call on the same stream.  Calls that
+ *    may run concurrently need distinct workspaces.  Errors found on the
+ *    device (non-finite input, a wait that ran out) are recorded in `ws`
+ *    and read with nvfp4_device_status;
+ *  - pointers must be 16-byte aligned and `ld` a multiple of 8 elements.
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_ARG = 1,         /* null pointer or bad enum value */
+    NVFP4_ERR_SHAPE = 2,       /* shape outside what the call supports */
+    NVFP4_ERR_ALIGN = 3,       /* pointer or leading dimension misaligned */
+    NVFP4_ERR_NONFINITE = 4,   /* input holds Inf or NaN (device-detected) */
+    NVFP4_ERR_TIMEOUT = 5,     /* a bounded device wait ran out (device-detected) */
+    NVFP4_ERR_CUDA = 6,        /* a CUDA runtime or driver call failed */
+    NVFP4_ERR_UNSUPPORTED = 7  /* device is not sm_103 / sm_100 family */
+} nvfp4_status;
+
+typedef enum { NVFP4_ROUND_RN = 0, NVFP4_ROUND_SR = 1 } nvfp4_round;
+typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_F32 = 1 } nvfp4_out_dtype;
+
+typedef void* nvfp4_stream_t; /* cudaStream_t */
+
+/* Bytes of the swizzled scale buffer for a rows x cols matrix (cols % 16 == 0). */
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
+
+/* Bytes of the device workspace (independent of the shapes given). */
+size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols);
+
+/* Zero a workspace on `stream` (needed once, and after any device error). */
+nvfp4_status nvfp4_workspace_init(void* ws, nvfp4_stream_t stream);
+
+/*
+ * 1x16 quantization along rows [16 contiguous elements share an E4M3 scale:
+ * "Entrenamiento ...", "Características del Formato NVFP4"; RN forward / SR
+ * backward: "FP4 All the Way", "Describir"].
+ *   x      bf16 [rows, cols], leading dimension ld (elements); cols % 16 == 0
+ *   mode   NVFP4_ROUND_RN or NVFP4_ROUND_SR; sr_seed keys the SR generator
+ *          (block index = row * cols/16 + col/16)
+ *   q      out: uint8 [rows, cols/2] packed codes
+ *   sf     out: nvfp4_sf_bytes(rows, cols) swizzled scale bytes
+ *   g_dec  out: one float, the tensor decode scale (device memory)
+ * One fused kernel: per-tensor amax, grid-wide barrier, block scales, codes.
+ */
+nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                            nvfp4_round mode, uint64_t sr_seed,
+                            uint8_t* q, uint8_t* sf, float* g_dec,
+                            void* ws, nvfp4_stream_t stream);
+
+/*
+ * 2-D 16x16 block quantization for weights ["Entrenamiento ...",
+ * "Metodología de Entrenamiento": two-dimensional block scaling for weights].
+ * One E4M3 scale per 16x16 tile, stored in each of the tile's 16 rows;
+ * round-to-nearest.  rows % 16 == 0, cols % 16 == 0.
+ *   q, sf   out: [rows, cols/2] codes and their scales (as nvfp4_quantize)
+ *   qT, sfT out (both NULL or both set): the transpose, [cols, rows/2] codes
+ *           and nvfp4_sf_bytes(cols, rows) scales — the K-major operand of
+ *           the gradient-wrt-input matmul.
+ */
+nvfp4_status nvfp4_quantize_2d(const void* w, int64_t rows, int64_t cols, int64_t ld,
+                               uint8_t* q, uint8_t* sf, uint8_t* qT, uint8_t* sfT,
+                               float* g_dec, void* ws, nvfp4_stream_t stream);
+
+/*
+ * Random Hadamard transform + quantization, written transposed, for the
+ * weight-gradient operands ["Entrenamiento ...", "Metodología de
+ * Entrenamiento": random Hadamard transforms; stochastic rounding on
+ * gradients].  For every channel c and 16-token chunk v of x [T, C]:
+ * y = (1/4) H16 D v, D = diag(±1) from rht_seed (the same for all chunks and
+ * for both operands of one weight-gradient matmul), butterflies with strides
+ * 1, 2, 4, 8.  amax runs over the transformed values.  T % 16 == 0.
+ *   qT  out: uint8 [C, T/2] codes, tokens contiguous (block index for SR =
+ *       c * T/16 + t/16)
+ *   sfT out: nvfp4_sf_bytes(C, T) scales
+ */
+nvfp4_status nvfp4_rht_quantize(const void* x, int64_t T, int64_t C, int64_t ld,
+                                uint64_t rht_seed, nvfp4_round mode, uint64_t sr_seed,
+                                uint8_t* qT, uint8_t* sfT, float* g_dec,
+                                void* ws, nvfp4_stream_t stream);
+
+/*
+ * Block-scaled NVFP4 matmul on the tcgen05 tensor cores [NVFP4 is supported
+ * by Blackwell tensor cores: "Entrenamiento ...", "El Desafío de la
+ * Precisión de 4 Bits"].
+ *   D[m, n] = ga * gb * sum_k A(m, k) B(n, k), A and B decoded NVFP4 (codes
+ *   times block scales), binary32 accumulation, output bf16 (round to
+ *   nearest) or binary32.
+ *   a, sfa  [M, K/2] codes + nvfp4_sf_bytes(M, K) scales (K contiguous)
+ *   b, sfb  [N, K/2] codes + nvfp4_sf_bytes(N, K) scales (K contiguous)
+ *   ga, gb  device floats (the quantizers' g_dec)
+ *   d       out: [M, N] row-major, leading dimension ldd (elements)
+ * Shapes: M % 128 == 0, N % 128 == 0, K % 64 == 0 (all > 0).
+ */
+nvfp4_status nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga,
+                        const uint8_t* b, const uint8_t* sfb, const float* gb,
+                        int64_t M, int64_t N, int64_t K,
+                        void* d, int64_t ldd, nvfp4_out_dtype out_dtype,
+                        void* ws, nvfp4_stream_t stream);
+
+/* Synchronise `stream` and return the sticky device status kept in `ws`
+ * (NVFP4_OK if no device-side error was recorded). */
+nvfp4_status nvfp4_device_status(void* ws, nvfp4_stream_t stream);
+
+/* Static string for a status code. */
+const char* nvfp4_status_str(nvfp4_status s);
+
+/*
+ * Diagnostic entry point: run the device's element encoders on n inputs —
+ * E4M3 nearest-even saturating (e4m3_out, for x >= 0), E2M1 nearest-even
+ * (e2m1_rn_out) and E2M1 stochastic with random byte r[i] (e2m1_sr_out) —
+ * the exact code paths the quantizers use.  Any output may be NULL.
+ */
+nvfp4_status nvfp4_encode_probe(const float* v, const uint8_t* r, int64_t n,
+                                uint8_t* e4m3_out, uint8_t* e2m1_rn_out, uint8_t* e2m1_sr_out,
+                                nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GB300_H */

@@ -1,0 +1,63 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4.h"
+
+namespace nvfp4 {
+
+// Device workspace (caller-owned, zeroed once).  The quantizers' grid-wide
+// barrier and amax live here; the last CTA of every call puts them back to 0.
+struct Workspace {
+    uint32_t status;      // sticky nvfp4_status recorded by the device (0 = OK)
+    uint32_t amax_bits;   // max |x| over the tensor, as float bits (atomicMax)
+    uint32_t arrived;     // CTAs that reached the grid barrier
+    uint32_t departed;    // CTAs that finished
+    uint32_t pad[60];
+};
+static_assert(sizeof(Workspace) == 256, "workspace layout");
+
+constexpr size_t kWorkspaceBytes = sizeof(Workspace);
+
+// Quantizer launch parameters (one struct for the three variants).
+struct QuantParams {
+    int64_t rows, cols;     // logical matrix of the input (rows x cols, or T x C)
+    int64_t ntiles;         // tiles in the whole tensor
+    int64_t tiles_c;        // tiles along the contiguous axis
+    uint8_t* q;             // codes
+    uint8_t* sf;            // scales
+    uint8_t* qT;            // transposed codes (2-D variant) or nullptr
+    uint8_t* sfT;           // transposed scales (2-D variant) or nullptr
+    float* g_dec;           // tensor decode scale out
+    uint64_t sr_seed;
+    uint32_t rht_signs;     // 16 sign bits (Hadamard variant)
+    int mode;               // nvfp4_round
+};
+
+enum class QuantKind { k1x16, k2d, kRht };
+
+// Host launchers (quantize.cu, gemm.cu, probe.cu).  They assume the
+// arguments were validated by the C-ABI layer.
+nvfp4_status launch_quantize(QuantKind kind, const void* x, int64_t ld, const QuantParams& p, Workspace* ws,
+                             cudaStream_t stream);
+
+nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
+                         const uint8_t* sfb, const float* gb, int64_t M, int64_t N, int64_t K, void* d,
+                         int64_t ldd, nvfp4_out_dtype dt, Workspace* ws, cudaStream_t stream);
+
+nvfp4_status launch_encode_probe(const float* v, const uint8_t* r, int64_t n, uint8_t* e4m3, uint8_t* rn,
+                                 uint8_t* sr, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).  Returns false if unavailable.
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t dim0,
+                          uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+                          CUtensorMapSwizzle swizzle);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace nvfp4

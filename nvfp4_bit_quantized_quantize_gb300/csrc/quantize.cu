@@ -1,0 +1,544 @@
+// Fused NVFP4 quantizers for sm_103a.
+//
+// One persistent, cooperative kernel per call does both levels of the
+// multi-level scaling ("I ricercatori di Nvidia ...", "Come funziona NVFP4?"):
+//   phase 1: stream the tensor through a TMA ring and reduce max |x|
+//            (max |RHT(x)| for the Hadamard variant);
+//   barrier: per-CTA maxima meet in the workspace; a bounded grid-wide
+//            barrier (cooperative launch guarantees co-residency);
+//   phase 2: per 16-element block: E4M3 block scale, element scaling,
+//            round-to-nearest or stochastic rounding onto E2M1, packed
+//            nibbles and swizzled scale bytes.
+// The last `stages` tiles a CTA read in phase 1 stay in shared memory and are
+// quantized first in phase 2 without a second HBM read; the rest are read
+// again in reverse order, so the most recently read tiles (likely still in
+// L2) come first.
+//
+// Tile ops:
+//   Op1x16 — 128 rows x 64 cols, 1x16 blocks along rows ("Entrenamiento ...",
+//            "Características del Formato NVFP4").
+//   Op2d   — same tile, one scale per 16x16 tile, optional transposed
+//            outputs ("Entrenamiento ...", "Metodología de Entrenamiento":
+//            two-dimensional block scaling for weights).
+//   OpRht  — 64 tokens x 128 channels, 16-point random Hadamard transform
+//            along tokens, quantized along tokens and written channel-major
+//            ("Metodología de Entrenamiento": random Hadamard transforms).
+//
+// Floating-point order is fixed and identical to the oracle: IEEE division
+// and multiplication with round-to-nearest (__fdiv_rn/__fmul_rn), no FMA
+// contraction in the scale math, the butterflies in stride order 1, 2, 4, 8.
+#include "device.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // last warp is the TMA producer
+constexpr int kTileBytes = 16384;
+constexpr int kMaxStages = 14;
+
+struct SmemCtl {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint32_t warp_amax[kConsumerWarps];
+    float amax;
+    int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kMaxStages * kTileBytes + sizeof(SmemCtl);
+
+// Swizzled (128-byte) address of 16-byte chunk `c` of row `r` in a tile whose
+// rows are 128 bytes.
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+
+// --------------------------------------------------------- block quantize ----
+// Scale and round one block of 16 binary32 values.  Returns the scale byte;
+// writes 8 bytes of packed codes.
+__device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], float bamax, float s_enc, int mode,
+                                                  uint64_t seed, uint64_t blk, uint32_t& lo32, uint32_t& hi32)
+{
+    const uint32_t sb = e4m3_rn_sat(__fmul_rn(__fdiv_rn(bamax, 6.0f), s_enc));
+    const float d = e4m3_value(sb);
+    uint32_t code[16];
+    if (d == 0.0f) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            code[j] = (__float_as_uint(x[j]) >> 28) & 8u;
+    } else {
+        const float f = __fdiv_rn(s_enc, d);
+        float v[16];
+        if (isinf(f)) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                v[j] = (x[j] == 0.0f) ? x[j] : __fmul_rn(x[j], f);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                v[j] = __fmul_rn(x[j], f);
+        }
+        if (mode == NVFP4_ROUND_SR) {
+            const U4 w = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, (uint32_t)seed,
+                                       (uint32_t)(seed >> 32));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                code[j] = e2m1_sr(v[j], (ws[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+        } else {
+            uint32_t bytes[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                bytes[j] = e2m1x2_rn(v[2 * j], v[2 * j + 1]);
+            lo32 = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+            hi32 = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+            return sb;
+        }
+    }
+    lo32 = 0;
+    hi32 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        lo32 |= code[j] << (4 * j);
+        hi32 |= code[8 + j] << (4 * j);
+    }
+    return sb;
+}
+
+// Tensor-level scales from amax (binary32): s_enc = 2688/amax saturated to
+// FLT_MAX, g = amax/2688; amax == 0 gives 0 for both.
+__device__ __forceinline__ void tensor_scales(float amax, float& s_enc, float& g)
+{
+    if (amax == 0.0f) {
+        s_enc = 0.0f;
+        g = 0.0f;
+        return;
+    }
+    s_enc = __fdiv_rn(2688.0f, amax);
+    if (isinf(s_enc))
+        s_enc = 3.402823466e38f;
+    g = __fdiv_rn(amax, 2688.0f);
+}
+
+// Scan a 128 x 64 bf16 tile for max |x| (bf16x2 accumulator, NaN-propagating).
+__device__ __forceinline__ uint32_t scan_tile_bf16(const uint8_t* tile, int ctid, uint32_t acc)
+{
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint32_t row = (uint32_t)(ctid >> 2) + 64u * k, blk = ctid & 3;
+        const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
+        const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
+        acc = habs_max2(acc, a.x); acc = habs_max2(acc, a.y);
+        acc = habs_max2(acc, a.z); acc = habs_max2(acc, a.w);
+        acc = habs_max2(acc, b.x); acc = habs_max2(acc, b.y);
+        acc = habs_max2(acc, b.z); acc = habs_max2(acc, b.w);
+    }
+    return acc;
+}
+
+// ------------------------------------------------------------------ 1x16 ----
+struct Op1x16 {
+    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
+                                 const QuantParams& p)
+    {
+        const int64_t tr = tile / p.tiles_c, tc = tile % p.tiles_c;
+        tma_load_2d(dst, m, bar, (int32_t)(tc * 64), (int32_t)(tr * 128));
+    }
+
+    __device__ static uint32_t phase1(const uint8_t* tile, int ctid, const QuantParams&)
+    {
+        return hmax_to_float_bits(scan_tile_bf16(tile, ctid, 0u));
+    }
+
+    __device__ static uint32_t hmax_to_float_bits(uint32_t acc) { return __float_as_uint(hmax_to_float(acc)); }
+
+    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const QuantParams& p)
+    {
+        const int64_t tr = t / p.tiles_c, tc = t % p.tiles_c;
+        const int lane = ctid & 31;
+        const int64_t kblocks = p.cols / 16;
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t row = (uint32_t)(ctid >> 2) + 64u * k, blk = ctid & 3;
+            const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
+            const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            float x[16];
+            uint32_t acc = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                x[2 * j] = bf16lo(w[j]);
+                x[2 * j + 1] = bf16hi(w[j]);
+                acc = habs_max2(acc, w[j]);
+            }
+            const int64_t grow = tr * 128 + row;
+            const int64_t gcol = tc * 64 + blk * 16;
+            uint32_t lo32, hi32;
+            const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc, p.mode, p.sr_seed,
+                                              (uint64_t)(grow * kblocks + gcol / 16), lo32, hi32);
+            if (grow < p.rows && gcol < p.cols)
+                *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
+            // the 4 blocks of this row sit in lanes 4i..4i+3: one 4-byte store
+            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
+            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
+            if ((lane & 3) == 0) {
+                const int64_t atom = (tr * p.tiles_c + tc) * 512;
+                *reinterpret_cast<uint32_t*>(p.sf + atom + (row & 31) * 16 + (row >> 5) * 4) =
+                    sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------- 2-D ----
+// In-register transpose of a 16 x 16 nibble matrix held by 16 lanes (lane i
+// holds row i, nibble j at bits 4j); afterwards lane j holds column j.
+__device__ __forceinline__ uint64_t nibble_transpose16(uint64_t w, int i)
+{
+    const uint64_t masks[4] = {0x00000000FFFFFFFFull, 0x0000FFFF0000FFFFull, 0x00FF00FF00FF00FFull,
+                               0x0F0F0F0F0F0F0F0Full};
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int k = 8 >> s;
+        const uint64_t mask = masks[s];
+        const bool upper = (i & k) != 0;
+        const uint64_t send = upper ? (w & mask) : ((w >> (4 * k)) & mask);
+        const uint32_t slo = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)send, k);
+        const uint32_t shi = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)(send >> 32), k);
+        const uint64_t recv = ((uint64_t)shi << 32) | slo;
+        w = upper ? ((w & ~mask) | recv) : ((w & mask) | (recv << (4 * k)));
+    }
+    return w;
+}
+
+struct Op2d {
+    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
+                                 const QuantParams& p)
+    {
+        Op1x16::issue(m, dst, bar, tile, p);
+    }
+
+    __device__ static uint32_t phase1(const uint8_t* tile, int ctid, const QuantParams& p)
+    {
+        return Op1x16::phase1(tile, ctid, p);
+    }
+
+    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const QuantParams& p)
+    {
+        const int64_t tr = t / p.tiles_c, tc = t % p.tiles_c;
+        const int lane = ctid & 31, cw = ctid >> 5;
+        const int64_t kblocksT = p.rows / 16;
+        const int64_t cpT = (kblocksT + 3) / 4;
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            const int P = k * 16 + cw * 2 + (lane >> 4);
+            const uint32_t g = P >> 2, blk = P & 3, i = lane & 15;
+            const uint32_t row = g * 16 + i;
+            const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
+            const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            float x[16];
+            uint32_t acc = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                x[2 * j] = bf16lo(w[j]);
+                x[2 * j + 1] = bf16hi(w[j]);
+                acc = habs_max2(acc, w[j]);
+            }
+            uint32_t m = __float_as_uint(hmax_to_float(acc));
+#pragma unroll
+            for (int off = 1; off < 16; off <<= 1)
+                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+            const int64_t grow = tr * 128 + row;
+            const int64_t gcol = tc * 64 + blk * 16;
+            uint32_t lo32, hi32;
+            const uint32_t sb = quant_block16(x, __uint_as_float(m), s_enc, NVFP4_ROUND_RN, 0, 0, lo32, hi32);
+            if (grow < p.rows && gcol < p.cols)
+                *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
+            p.sf[(tr * p.tiles_c + tc) * 512 + (row & 31) * 16 + (row >> 5) * 4 + blk] = (uint8_t)sb;
+            if (p.qT != nullptr) {
+                const uint64_t col = nibble_transpose16(((uint64_t)hi32 << 32) | lo32, (int)i);
+                const int64_t rT = gcol + i;          // row of the transposed matrix
+                const int64_t kbT = tr * 8 + g;       // its 16-block index
+                if (rT < p.cols && kbT < kblocksT)
+                    *reinterpret_cast<uint2*>(p.qT + rT * (p.rows / 2) + kbT * 8) =
+                        make_uint2((uint32_t)col, (uint32_t)(col >> 32));
+                if (kbT < 4 * cpT)
+                    p.sfT[((rT >> 7) * cpT + (kbT >> 2)) * 512 + (rT & 31) * 16 + ((rT & 127) >> 5) * 4 +
+                          (kbT & 3)] = (uint8_t)sb;
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------- RHT ----
+struct OpRht {
+    // tile = 64 tokens x 128 channels as two 64 x 64 boxes (8 KB each)
+    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
+                                 const QuantParams& p)
+    {
+        const int64_t tt = tile / p.tiles_c, ct = tile % p.tiles_c;
+        tma_load_2d(dst, m, bar, (int32_t)(ct * 128), (int32_t)(tt * 64));
+        tma_load_2d(dst + 8192, m, bar, (int32_t)(ct * 128 + 64), (int32_t)(tt * 64));
+    }
+
+    // y = (1/4) H16 D v for the two channels held by this thread.
+    __device__ static void transform(const uint8_t* tile, int ctid, uint32_t signs, float (&y0)[16],
+                                     float (&y1)[16])
+    {
+        const int lane = ctid & 31, cw = ctid >> 5;
+        const uint32_t tb = cw >> 1, h = cw & 1;
+        const uint8_t* half = tile + h * 8192;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t row = tb * 16 + i;
+            const uint32_t w =
+                *reinterpret_cast<const uint32_t*>(half + sw128(row, (uint32_t)lane >> 2) + (lane & 3) * 4);
+            const uint32_t flip = ((signs >> i) & 1u) << 31;
+            y0[i] = __uint_as_float((w << 16) ^ flip);
+            y1[i] = __uint_as_float((w & 0xFFFF0000u) ^ flip);
+        }
+#pragma unroll
+        for (int hs = 1; hs < 16; hs <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (i & hs)
+                    continue;
+                const float a0 = y0[i], b0 = y0[i + hs];
+                y0[i] = __fadd_rn(a0, b0);
+                y0[i + hs] = __fsub_rn(a0, b0);
+                const float a1 = y1[i], b1 = y1[i + hs];
+                y1[i] = __fadd_rn(a1, b1);
+                y1[i + hs] = __fsub_rn(a1, b1);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            y0[i] = __fmul_rn(y0[i], 0.25f);
+            y1[i] = __fmul_rn(y1[i], 0.25f);
+        }
+    }
+
+    __device__ static uint32_t phase1(const uint8_t* tile, int ctid, const QuantParams& p)
+    {
+        float y0[16], y1[16];
+        transform(tile, ctid, p.rht_signs, y0, y1);
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            m = max(m, __float_as_uint(y0[i]) & 0x7FFFFFFFu);
+            m = max(m, __float_as_uint(y1[i]) & 0x7FFFFFFFu);
+        }
+        return m;
+    }
+
+    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const QuantParams& p)
+    {
+        const int64_t tt = t / p.tiles_c, ct = t % p.tiles_c;
+        const int lane = ctid & 31, cw = ctid >> 5;
+        const uint32_t tb = cw >> 1, h = cw & 1;
+        const int64_t T = p.rows, C = p.cols;
+        const int64_t kblocks = T / 16;
+        const int64_t cp = (kblocks + 3) / 4;
+        float y[2][16];
+        transform(tile, ctid, p.rht_signs, y[0], y[1]);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+            float bamax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                bamax = fmaxf(bamax, fabsf(y[ch][i]));
+            const uint32_t cl = h * 64 + 2 * lane + ch;  // channel within tile
+            const int64_t c = ct * 128 + cl;
+            const int64_t kb = tt * 4 + tb;
+            uint32_t lo32, hi32;
+            const uint32_t sb =
+                quant_block16(y[ch], bamax, s_enc, p.mode, p.sr_seed, (uint64_t)(c * kblocks + kb), lo32, hi32);
+            if (c < C && kb < kblocks)
+                *reinterpret_cast<uint2*>(p.q + c * (T / 2) + kb * 8) = make_uint2(lo32, hi32);
+            p.sf[(ct * cp + tt) * 512 + (cl & 31) * 16 + (cl >> 5) * 4 + tb] = (uint8_t)sb;
+        }
+    }
+};
+
+// ---------------------------------------------------------------- kernel ----
+template <class Op>
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, Workspace* ws,
+                          int stages)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (size_t)kMaxStages * kTileBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t G = gridDim.x, bid = blockIdx.x;
+    const int64_t t_begin = p.ntiles * bid / G, t_end = p.ntiles * (bid + 1) / G;
+    const int64_t n = t_end - t_begin;
+    const int64_t R = n < stages ? n : stages;  // tiles kept on chip across the barrier
+    const int64_t total_loads = 2 * n - R;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMaxStages; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], kConsumerWarps);
+        }
+        ctl->abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer ----
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap);
+            int64_t issued = 0;
+            for (int64_t i = 0; i < total_loads; ++i) {
+                const int s = (int)(i % stages);
+                if (i >= stages && !mbar_wait(&ctl->empty[s], (uint32_t)(((i / stages) - 1) & 1), ws, &ctl->abort))
+                    break;
+                const int64_t tile = (i < n) ? t_begin + i : t_begin + (n - R - 1) - (i - n);
+                mbar_expect_tx(&ctl->full[s], kTileBytes);
+                Op::issue(&tmap, smem + (size_t)s * kTileBytes, &ctl->full[s], tile, p);
+                ++issued;
+            }
+            // never leave with copies in flight
+            for (int64_t i = issued > stages ? issued - stages : 0; i < issued; ++i)
+                mbar_wait(&ctl->full[i % stages], (uint32_t)((i / stages) & 1), ws, nullptr);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers ----
+    const int ctid = threadIdx.x;  // 0 .. kConsumers-1
+    uint32_t amax_bits = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int s = (int)(i % stages);
+        if (!mbar_wait(&ctl->full[s], (uint32_t)((i / stages) & 1), ws, &ctl->abort))
+            break;
+        amax_bits = max(amax_bits, Op::phase1(smem + (size_t)s * kTileBytes, ctid, p));
+        if (i < n - R) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ctl->empty[s]);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, off));
+    if (lane == 0)
+        ctl->warp_amax[warp] = amax_bits;
+    named_bar_sync(1, kConsumers);
+    if (ctid == 0) {
+        uint32_t m = 0;
+        for (int w = 0; w < kConsumerWarps; ++w)
+            m = max(m, ctl->warp_amax[w]);
+        atomicMax(&ws->amax_bits, m);
+        __threadfence();
+        atomicAdd(&ws->arrived, 1u);
+        const uint64_t t0 = global_ns();
+        while (ld_acquire_gpu(&ws->arrived) < (uint32_t)G) {
+            if (global_ns() - t0 > kWaitLimitNs) {
+                record_status(ws, NVFP4_ERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(64);
+        }
+        const uint32_t am = ld_acquire_gpu(&ws->amax_bits);
+        if (am >= 0x7F800000u)
+            record_status(ws, NVFP4_ERR_NONFINITE);
+        ctl->amax = __uint_as_float(am);
+    }
+    named_bar_sync(1, kConsumers);
+
+    float s_enc, g;
+    tensor_scales(ctl->amax, s_enc, g);
+    if (bid == 0 && ctid == 0)
+        *p.g_dec = g;
+
+    volatile int* abort_flag = &ctl->abort;
+    for (int64_t j = 0; j < n && !*abort_flag; ++j) {
+        const int64_t i = (j < R) ? (n - R + j) : (n + j - R);
+        const int s = (int)(i % stages);
+        if (j >= R && !mbar_wait(&ctl->full[s], (uint32_t)((i / stages) & 1), ws, &ctl->abort))
+            break;
+        const int64_t tile = (j < R) ? t_begin + n - R + j : t_begin + (n - R - 1) - (j - R);
+        Op::phase2(smem + (size_t)s * kTileBytes, tile, ctid, s_enc, p);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&ctl->empty[s]);
+    }
+
+    named_bar_sync(1, kConsumers);
+    if (ctid == 0) {
+        __threadfence();
+        const uint32_t old = atomicAdd(&ws->departed, 1u);
+        if (old == (uint32_t)G - 1) {
+            ws->amax_bits = 0;
+            ws->arrived = 0;
+            ws->departed = 0;
+            __threadfence();
+        }
+    }
+}
+
+template <class Op>
+nvfp4_status launch_fused(const CUtensorMap& map, const QuantParams& p, Workspace* ws, cudaStream_t stream)
+{
+    auto kern = fused_quantize_kernel<Op>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, kSmemBytes) != cudaSuccess || occ < 1)
+        return NVFP4_ERR_CUDA;
+    const int64_t max_grid = (int64_t)occ * device_sm_count();
+    const int grid = (int)(p.ntiles < max_grid ? p.ntiles : max_grid);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int stages = kMaxStages;
+    if (cudaLaunchKernelEx(&cfg, kern, map, p, ws, stages) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    return NVFP4_OK;
+}
+
+}  // namespace
+
+nvfp4_status launch_quantize(QuantKind kind, const void* x, int64_t ld, const QuantParams& p, Workspace* ws,
+                             cudaStream_t stream)
+{
+    CUtensorMap map;
+    const bool ok = encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(x),
+                                         (uint64_t)p.cols, (uint64_t)p.rows, (uint64_t)ld * 2u,
+                                         kind == QuantKind::kRht ? 64u : 64u, kind == QuantKind::kRht ? 64u : 128u,
+                                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok)
+        return NVFP4_ERR_CUDA;
+    switch (kind) {
+    case QuantKind::k1x16:
+        return launch_fused<Op1x16>(map, p, ws, stream);
+    case QuantKind::k2d:
+        return launch_fused<Op2d>(map, p, ws, stream);
+    case QuantKind::kRht:
+        return launch_fused<OpRht>(map, p, ws, stream);
+    }
+    return NVFP4_ERR_ARG;
+}
+
+}  // namespace nvfp4

@@ -181,15 +181,17 @@ void or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out
     memcpy(out, c, sizeof c);
 }
 
-/* Random byte for lane j of output block blk (reading): Philox with
- * key = seed, counter = (blk lo, blk hi, 0, 0); byte j of the 128-bit result. */
-static unsigned sr_byte(uint64_t seed, uint64_t blk, int j)
+/* Random bytes of output block blk (reading): Philox with key = seed,
+ * counter = (blk lo, blk hi, 0, 0); lane j of the block takes byte j of the
+ * 128-bit result (bytes of word 0 first, least significant first). */
+static void sr_bytes(uint64_t seed, uint64_t blk, unsigned r[16])
 {
     uint32_t ctr[4] = {(uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u};
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t w[4];
     or_philox4x32_10(ctr, key, w);
-    return (w[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+    for (int j = 0; j < 16; ++j)
+        r[j] = (w[j >> 2] >> (8 * (j & 3))) & 0xFFu;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -296,13 +298,16 @@ static void quantize_block(const float x[16], float s_enc, int sb, int mode,
 {
     float d = or_e4m3_value(sb);
     float f = (d == 0.0f) ? 0.0f : s_enc / d;
+    unsigned r[16] = {0};
+    if (mode == 1)
+        sr_bytes(seed, blk, r);
     for (int j = 0; j < 16; ++j) {
         float v;
         if (d == 0.0f || x[j] == 0.0f)
             v = signbit(x[j]) ? -0.0f : 0.0f;
         else
             v = x[j] * f;
-        codes[j] = (mode == 1) ? or_e2m1_sr(v, sr_byte(seed, blk, j)) : or_e2m1_rn(v);
+        codes[j] = (mode == 1) ? or_e2m1_sr(v, r[j]) : or_e2m1_rn(v);
     }
 }
 

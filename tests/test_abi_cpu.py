@@ -1,0 +1,77 @@
+"""C-ABI checks that need no GPU: the library builds/loads, exports every
+function include/*.h declares, and rejects bad arguments on the host before
+touching the device."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import nvfp4_bit_quantized_quantize_gb300 as nv
+from nvfp4_bit_quantized_quantize_gb300 import build as nvbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(nvfp4_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nvbuild.build()
+    return nv.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ["nvfp4_quantize", "nvfp4_quantize_2d", "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_sf_bytes",
+              "nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_device_status", "nvfp4_status_str"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", nv.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (nvfp4_\w+)$", out, flags=re.M))
+    declared = _declared()
+    assert declared, "no declarations found"
+    assert declared <= exported, declared - exported
+    assert set(nv.EXPORTS) == declared
+    for n in declared:
+        assert hasattr(lib, n)
+
+
+def test_sizes_and_status_strings(lib):
+    assert nv.nvfp4_sf_bytes(256, 256) == 256 * 16
+    assert nv.nvfp4_sf_bytes(1, 16) == 512
+    assert nv.nvfp4_sf_bytes(129, 1040) == 256 * 68
+    assert nv.nvfp4_workspace_bytes() == 256
+    assert nv.nvfp4_status_str(0) == "ok"
+    assert nv.nvfp4_status_str(4) == "non-finite input"
+
+
+def test_host_validation_rejects_before_launch(lib):
+    # null pointers and bad shapes return synchronously, no device touched
+    L = lib
+    fake = 1 << 20  # aligned, never dereferenced
+    assert L.nvfp4_quantize(None, 16, 16, 16, 0, 0, fake, fake, fake, fake, None) == 1
+    assert L.nvfp4_quantize(fake, 16, 16, 16, 7, 0, fake, fake, fake, fake, None) == 1
+    assert L.nvfp4_quantize(fake, 16, 24, 24, 0, 0, fake, fake, fake, fake, None) == 2
+    assert L.nvfp4_quantize(fake, 0, 16, 16, 0, 0, fake, fake, fake, fake, None) == 2
+    assert L.nvfp4_quantize(fake + 8, 16, 16, 16, 0, 0, fake, fake, fake, fake, None) == 3
+    assert L.nvfp4_quantize(fake, 16, 32, 36, 0, 0, fake, fake, fake, fake, None) == 3
+    assert L.nvfp4_quantize_2d(fake, 24, 32, 32, fake, fake, fake, None, fake, fake, None) == 1
+    assert L.nvfp4_quantize_2d(fake, 24, 32, 32, fake, fake, None, None, fake, fake, None) == 2
+    assert L.nvfp4_rht_quantize(fake, 24, 32, 32, 1, 0, 0, fake, fake, fake, fake, None) == 2
+    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 100, 128, 64, fake, 128, 0, fake, None) == 2
+    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 128, 128, 96, fake, 128, 0, fake, None) == 2
+    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 128, 128, 64, fake, 128, 5, fake, None) == 1
+    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 128, 128, 64, fake, 132, 0, fake, None) == 3
+    assert L.nvfp4_workspace_init(None, None) == 1

@@ -1,0 +1,162 @@
+"""Quantizer parity: the CUDA kernels against the oracle, bit for bit (codes,
+raw swizzled scale bytes including padding, and the binary32 tensor scale)."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import nvfp4_bit_quantized_quantize_gb300 as nv
+from nvfp4_bit_quantized_quantize_gb300 import synth
+
+from gpu_helpers import quantize, quantize_2d, rht_quantize
+
+pytestmark = pytest.mark.gpu
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")))
+
+
+def _assert_same(gpu, ref, what):
+    g = np.asarray(gpu)
+    r = np.asarray(ref)
+    assert g.shape == r.shape, what
+    bad = np.flatnonzero(g.ravel() != r.ravel())
+    assert bad.size == 0, f"{what}: {bad.size} mismatches, first at {bad[:8]}: gpu {g.ravel()[bad[:8]]} ref {r.ravel()[bad[:8]]}"
+
+
+SHAPES = [(256, 256), (1, 16), (16, 48), (200, 80), (130, 1040), (384, 192), (1024, 1024)]
+
+
+@pytest.mark.parametrize("mode", [nv.RN, nv.SR])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_quantize_1x16_parity(shape, mode):
+    x = synth.normal_bf16(shape, 11, shape[0] % 7, 1.0, 0.0, 0.005, 50.0)
+    q, sf, g, st = quantize(x, mode, seed=1234)
+    rq, rsf, rg = O.quantize(x, mode, 1234)
+    assert st == 0
+    assert np.float32(g) == np.float32(rg)
+    _assert_same(q, rq, "codes")
+    _assert_same(sf, rsf, "scales")
+
+
+def test_quantize_leading_dimension_and_workspace_reuse():
+    x = synth.normal_bf16((136, 96), 5, 0)
+    ws = nv.alloc_workspace()
+    for mode in (nv.RN, nv.SR, nv.RN):
+        q, sf, g, st = quantize(x, mode, seed=7, ld=136, ws=ws)
+        rq, rsf, rg = O.quantize(x, mode, 7)
+        assert st == 0 and g == rg
+        _assert_same(q, rq, "codes")
+        _assert_same(sf, rsf, "scales")
+
+
+def test_worked_examples_on_gpu():
+    e1, e2 = GOLD["E1"], GOLD["E2"]
+    x = synth.f32_to_bf16_bits(np.array([[float(s) for s in e1["x"] + e2["x"]]], np.float32))
+    q, sf, g, st = quantize(x, nv.RN)
+    assert st == 0
+    assert q[0, :8].tobytes().hex() == e1["packed_hex"]
+    assert q[0, 8:].tobytes().hex() == e2["packed_hex"]
+    assert sf[0] == int(e1["scale_byte"], 16) and sf[1] == int(e2["scale_byte"], 16)
+    assert np.float32(g).view(np.uint32) == int(e1["g_f32_hex"], 16)
+
+
+def test_zero_tensor_and_signed_zero():
+    x = synth.f32_to_bf16_bits(np.array([[0.0] * 8 + [-0.0] * 8] * 3, np.float32))
+    for mode in (nv.RN, nv.SR):
+        q, sf, g, st = quantize(x, mode, 3)
+        assert st == 0 and g == 0.0
+        assert np.all(sf == 0)
+        assert q[0].tobytes().hex() == "0000000088888888"
+
+
+def test_tiny_values_and_saturating_scales():
+    # amax in the bf16 subnormal range: s_enc saturates to FLT_MAX; zeros stay zero
+    x = np.zeros((4, 32), np.float32)
+    x[0, :5] = [2.0 ** -133, -2.0 ** -130, 2.0 ** -127, 0.0, -0.0]
+    x[3, 17] = 2.0 ** -126
+    xb = synth.f32_to_bf16_bits(x)
+    for mode in (nv.RN, nv.SR):
+        q, sf, g, st = quantize(xb, mode, 9)
+        rq, rsf, rg = O.quantize(xb, mode, 9)
+        assert st == 0 and g == rg
+        _assert_same(q, rq, "codes")
+        _assert_same(sf, rsf, "scales")
+
+
+def test_nonfinite_input_is_reported():
+    x = synth.normal_bf16((64, 64), 3, 0)
+    x[5, 7] = 0x7F80  # +inf
+    _, _, _, st = quantize(x)
+    assert st == 4
+    x[5, 7] = 0xFFC1  # NaN
+    _, _, _, st = quantize(x)
+    assert st == 4
+
+
+@pytest.mark.parametrize("shape", [(256, 256), (48, 80), (144, 208), (16, 16), (512, 1024)])
+def test_quantize_2d_parity(shape):
+    w = synth.normal_bf16(shape, 21, 0, 0.02, 0.0, 0.002, 100.0)
+    q, sf, qT, sfT, g, st = quantize_2d(w)
+    rq, rsf, rqT, rsfT, rg = O.quantize_2d(w)
+    assert st == 0 and g == rg
+    _assert_same(q, rq, "codes")
+    _assert_same(sf, rsf, "scales")
+    _assert_same(qT, rqT, "transposed codes")
+    _assert_same(sfT, rsfT, "transposed scales")
+
+
+def test_quantize_2d_without_transpose():
+    w = synth.normal_bf16((96, 64), 22, 0, 0.02)
+    q, sf, _, _, g, st = quantize_2d(w, transpose=False)
+    rq, rsf, _, _, rg = O.quantize_2d(w, transpose=False)
+    assert st == 0 and g == rg
+    _assert_same(q, rq, "codes")
+    _assert_same(sf, rsf, "scales")
+
+
+@pytest.mark.parametrize("mode", [nv.RN, nv.SR])
+@pytest.mark.parametrize("shape", [(64, 128), (48, 40), (272, 200), (16, 8), (1024, 384)])
+def test_rht_quantize_parity(shape, mode):
+    x = synth.normal_bf16(shape, 31, 1, 1e-3 if mode == nv.SR else 1.0)
+    qT, sfT, g, st = rht_quantize(x, rht_seed=77, mode=mode, sr_seed=5)
+    rqT, rsfT, rg = O.rht_quantize(x, 77, mode, 5)
+    assert st == 0 and g == rg
+    _assert_same(qT, rqT, "codes")
+    _assert_same(sfT, rsfT, "scales")
+
+
+# ---------------------------------------------- full-size workload tensors ----
+
+@pytest.mark.parametrize("name", ["A1024", "A4096", "A8192"])
+def test_quantize_sweep_full_size(name):
+    x = synth.make_workload("quantize_sweep", only={name})[name]
+    seed = synth.WORKLOADS["quantize_sweep"]["seed"]
+    for mode in (nv.RN, nv.SR):
+        q, sf, g, st = quantize(x, mode, seed)
+        rq, rsf, rg = O.quantize(x, mode, seed)
+        assert st == 0 and g == rg
+        _assert_same(q, rq, "codes")
+        _assert_same(sf, rsf, "scales")
+
+
+def test_weight_2d_full_size_fprop_workload():
+    w = synth.make_workload("fprop_w2d_8192x20480x5120", only={"W"})["W"]
+    q, sf, qT, sfT, g, st = quantize_2d(w)
+    rq, rsf, rqT, rsfT, rg = O.quantize_2d(w)
+    assert st == 0 and g == rg
+    _assert_same(q, rq, "codes")
+    _assert_same(sf, rsf, "scales")
+    _assert_same(qT, rqT, "transposed codes")
+    _assert_same(sfT, rsfT, "transposed scales")
+
+
+def test_rht_sr_full_size_wgrad_workload():
+    wl = synth.make_workload("wgrad_rht_sr_16384x5120", only={"dY"})
+    seed = synth.WORKLOADS["wgrad_rht_sr_16384x5120"]["seed"]
+    qT, sfT, g, st = rht_quantize(wl["dY"], rht_seed=seed + 1, mode=nv.SR, sr_seed=seed)
+    rqT, rsfT, rg = O.rht_quantize(wl["dY"], seed + 1, O.SR, seed)
+    assert st == 0 and g == rg
+    _assert_same(qT, rqT, "codes")
+    _assert_same(sfT, rsfT, "scales")
