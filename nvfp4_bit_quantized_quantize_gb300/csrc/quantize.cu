@@ -263,9 +263,17 @@ struct Op2d {
                 if (rT < p.cols && kbT < kblocksT)
                     *reinterpret_cast<uint2*>(p.qT + rT * (p.rows / 2) + kbT * 8) =
                         make_uint2((uint32_t)col, (uint32_t)(col >> 32));
-                if (kbT < 4 * cpT)
+                if (kbT < 4 * cpT) {
                     p.sfT[((rT >> 7) * cpT + (kbT >> 2)) * 512 + (rT & 31) * 16 + ((rT & 127) >> 5) * 4 +
                           (kbT & 3)] = (uint8_t)sb;
+                    // an odd count of 64-column tiles leaves the upper half of
+                    // the last 128-row scale atom to padding: write its zeros
+                    if ((p.tiles_c & 1) && tc == p.tiles_c - 1) {
+                        const int64_t rP = rT + 64;
+                        p.sfT[((rP >> 7) * cpT + (kbT >> 2)) * 512 + (rP & 31) * 16 + ((rP & 127) >> 5) * 4 +
+                              (kbT & 3)] = 0;
+                    }
+                }
             }
         }
     }
