@@ -174,6 +174,40 @@ nvfp4_status nvfp4_encode_probe(const float* v, const uint8_t* r, int64_t n,
                                 uint8_t* e4m3_out, uint8_t* e2m1_rn_out, uint8_t* e2m1_sr_out,
                                 nvfp4_stream_t stream);
 
+/*
+ * nvfp4_quantize_noalloc — the 1x16 quantizer of nvfp4_quantize for callers
+ * that cannot allocate device memory.  (The pages have no counterpart; this
+ * is an interface convenience.)
+ *
+ * Who needs it: code that may not call cudaMalloc or any allocating routine —
+ * a plugin running inside a host program that owns all device memory through
+ * its own allocator, a deployment that reserves the whole device at start-up,
+ * or a latency-critical path where an allocation could block or synchronise
+ * the device.  nvfp4_quantize wants a caller-allocated workspace; this variant
+ * keeps that scratch in a 256-byte static device array inside the library
+ * instead, so the caller passes only the input and the outputs.
+ *
+ * Arguments, layouts and results are those of nvfp4_quantize (same kernel,
+ * same bits).  Differences:
+ *  - no workspace: the scratch is a file-scope device array of 256 bytes,
+ *    held by every GPU that loads the library until the process exits; a
+ *    shape whose workspace (nvfp4_workspace_bytes) would exceed it returns
+ *    NVFP4_ERR_SHAPE;
+ *  - nothing is allocated: no cudaMalloc/cudaFree, no allocating library call;
+ *  - each call clears the scratch on `stream` before its launch; all calls
+ *    share the one array, so calls that overlap on the GPU (e.g. on two
+ *    streams at once) race — serialise them, e.g. on one stream;
+ *  - the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture begins;
+ *  - device-detected errors are not kept anywhere the caller can query; a
+ *    non-finite input shows up as a non-finite *g_dec.
+ */
+nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                    nvfp4_round mode, uint64_t sr_seed,
+                                    uint8_t* q, uint8_t* sf, float* g_dec,
+                                    nvfp4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ STATUS = {0: "OK", 1: "ERR_ARG", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_NONFINI
 
 EXPORTS = ["nvfp4_sf_bytes", "nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_quantize",
            "nvfp4_quantize_2d", "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_device_status",
-           "nvfp4_status_str", "nvfp4_encode_probe"]
+           "nvfp4_status_str", "nvfp4_encode_probe", "nvfp4_quantize_noalloc"]
 
 
 class NVFP4Error(RuntimeError):
@@ -58,6 +58,7 @@ def load() -> ctypes.CDLL:
         "nvfp4_device_status": ([p, p], i32),
         "nvfp4_status_str": ([i32], ctypes.c_char_p),
         "nvfp4_encode_probe": ([p, p, i64, p, p, p, p], i32),
+        "nvfp4_quantize_noalloc": ([p, i64, i64, i64, i32, u64, p, p, p, p], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -137,6 +138,13 @@ def nvfp4_status_str(status: int) -> str:
 def nvfp4_encode_probe(v, r, n, e4m3_out, e2m1_rn_out, e2m1_sr_out, stream=None) -> None:
     _check("nvfp4_encode_probe", load().nvfp4_encode_probe(
         _ptr(v), _ptr(r), n, _ptr(e4m3_out), _ptr(e2m1_rn_out), _ptr(e2m1_sr_out), _stream(stream)))
+
+
+def nvfp4_quantize_noalloc(x, rows, cols, ld, mode, sr_seed, q, sf, g_dec, stream=None) -> None:
+    """nvfp4_quantize without a workspace, for callers that cannot allocate
+    device memory: the library keeps the scratch in a static device array."""
+    _check("nvfp4_quantize_noalloc", load().nvfp4_quantize_noalloc(
+        _ptr(x), rows, cols, ld, mode, sr_seed, _ptr(q), _ptr(sf), _ptr(g_dec), _stream(stream)))
 
 
 # ------------------------------------------------------- output allocation ----
