@@ -115,6 +115,22 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// TMA store of a 2-D box from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most 0 bulk groups still read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Make generic-proxy shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // -------------------------------------------------------------- tcgen05 ----
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -280,24 +296,34 @@ __device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi)
     return r;
 }
 
-// Stochastic rounding of v onto the E2M1 grid with random byte r: with
-// a = |v| between grid neighbours lo and lo + gap, round up iff
-// r + 0.5 < t, t = 256 (a - lo) / gap (exact in binary32).  Saturates at 6,
-// keeps the sign.  Returns the 4-bit code.
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r)
+// Stochastic rounding of v onto the E2M1 grid.  With a = |v| between grid
+// neighbours lo and lo + gap (gap 0.5 below 2, 1 below 4, else 2), round up
+// iff r + 0.5 < t, t = 256 (a - lo) / gap, for the random byte r.  Every step
+// is exact in binary32: s = a / gap is a power-of-two scaling, s - floor(s) is
+// exact, and the result is a small integer times gap.  Saturates at 6 (also
+// for Inf/NaN magnitudes); keeps the sign.  `thr` is r + 0.5 as a float.
+__device__ __forceinline__ float sr_grid_value(float v, float thr)
 {
     const float a = fabsf(v);
-    const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
-    // grid spacing and the 256/gap factor by range
+    const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
     const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-    const float inv = a < 2.0f ? 512.0f : (a < 4.0f ? 256.0f : 128.0f);
-    const float lo = floorf(a * (inv * (1.0f / 256.0f))) * gap;   // exact
-    const float t = (a - lo) * inv;                                // exact
-    const float thr = (float)r + 0.5f;
-    float q = (thr < t) ? lo + gap : lo;
-    q = a < 6.0f ? q : 6.0f;
-    // q is exactly representable: encode with the nearest-even convert
-    return (e2m1x2_rn(q, 0.0f) & 7u) | sign;
+    const float s = a * inv;
+    const float fl = floorf(s);
+    const float t = (s - fl) * 256.0f;
+    const float q = fminf((thr < t ? fl + 1.0f : fl) * gap, 6.0f);
+    return copysignf(q, v);
+}
+
+// r + 0.5 for byte j (0..3) of w, exactly: the float 2^23 + r minus 2^23 - 0.5.
+__device__ __forceinline__ float sr_threshold(uint32_t w, uint32_t j)
+{
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | j)) - 8388607.5f;
+}
+
+// 4-bit code of the stochastic rounding of v with random byte r.
+__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r)
+{
+    return e2m1x2_rn(sr_grid_value(v, sr_threshold(r & 0xFFu, 0)), 0.0f) & 15u;
 }
 
 }  // namespace nvfp4

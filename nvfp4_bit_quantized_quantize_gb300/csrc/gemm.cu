@@ -12,8 +12,14 @@
 //   warp 1  allocates tensor memory, moves the scale atoms into it
 //           (tcgen05.cp) and issues tcgen05.mma.kind::mxf4nvf4 (K = 64 per
 //           instruction, binary32 accumulator in tensor memory);
-//   warps 2-5 epilogue: tcgen05.ld of the accumulator, times ga*gb, round to
-//           bf16 (or keep binary32), store.
+//   warps 2-9 epilogue, two per tensor-memory lane quarter (128 columns
+//           each): all tcgen05.ld of the accumulator issued before one wait,
+//           the accumulator released, then times ga*gb, round to bf16 (or
+//           keep binary32), and 32-row chunks staged in a 1 KB shared buffer
+//           per warp leave through TMA bulk tensor stores (per-thread row
+//           stores would flood the memory pipe the MMA warp issues through).
+// The MMA warp's issue loop is kept lean: every descriptor is a precomputed
+// base plus a constant offset, the four K = 64 steps of a stage are unrolled.
 // Every wait is bounded; a wait that runs out records NVFP4_ERR_TIMEOUT and
 // all roles wind down, drain their asynchronous work, and free tensor memory.
 #include "device.cuh"
@@ -30,7 +36,8 @@ constexpr int kBBytes = BN * BK / 2;          // 32 KB
 constexpr int kSfaBytes = (BM / 128) * (BK / 64) * 512;  // 2 KB
 constexpr int kSfbBytes = (BN / 128) * (BK / 64) * 512;  // 4 KB
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-constexpr int kThreads = 192;
+constexpr int kEpilogueWarps = 8;
+constexpr int kThreads = (2 + kEpilogueWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = BN;             // fp32 accumulator: 128 lanes x 256 columns
 constexpr uint32_t kSfColsPerStage = 16 + 32; // SFA 4 steps x 4 cols, SFB 4 steps x 8 cols
@@ -48,7 +55,8 @@ struct GemmCtl {
     int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(GemmCtl);
+constexpr int kStoreBufBytes = 1024;  // per epilogue warp: 32 rows x 32 bytes
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kEpilogueWarps * kStoreBufBytes + sizeof(GemmCtl);
 
 // Instruction descriptor for kind::mxf4nvf4: E2M1 A and B (format 1),
 // K-major both, N >> 3 at bit 17, E4M3 scales (bit 23 = 0), M >> 4 at bit 24,
@@ -61,8 +69,9 @@ struct GemmArgs {
     const float* ga;
     const float* gb;
     void* d;
-    int64_t M, N, K, ldd;
-    int out_f32;
+    int64_t ldd;
+    int32_t M, N, K;
+    int32_t out_f32;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -73,19 +82,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                     const GemmArgs args, Workspace* ws)
+                     const __grid_constant__ CUtensorMap tma_d, const GemmArgs args, Workspace* ws)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    GemmCtl* ctl = reinterpret_cast<GemmCtl*>(smem + (size_t)kStages * kStageBytes);
+    uint8_t* store_buf = smem + (size_t)kStages * kStageBytes;
+    GemmCtl* ctl = reinterpret_cast<GemmCtl*>(store_buf + kEpilogueWarps * kStoreBufBytes);
     volatile int* abort = &ctl->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t tiles_m = args.M / BM;
-    const int64_t tiles_n = (args.N + BN - 1) / BN;
-    const int64_t ntiles = tiles_m * tiles_n;
-    const int64_t kstages = (args.K + BK - 1) / BK;
-    const int64_t cp = (args.K / 16 + 3) / 4;   // scale atoms along K
+    const uint32_t tiles_m = (uint32_t)args.M / BM;
+    const uint32_t tiles_n = ((uint32_t)args.N + BN - 1) / BN;
+    const uint32_t ntiles = tiles_m * tiles_n;
+    const uint32_t kstages = ((uint32_t)args.K + BK - 1) / BK;
+    const uint32_t cp = ((uint32_t)args.K / 16 + 3) / 4;  // scale atoms along K
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -93,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->empty[s], 1);
         }
         mbar_init(&ctl->tmem_full, 1);
-        mbar_init(&ctl->tmem_empty, 4);
+        mbar_init(&ctl->tmem_empty, kEpilogueWarps);
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
         fence_mbar_init();
@@ -110,61 +120,93 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------- TMA producer ----
         tma_prefetch_desc(&tma_a);
         tma_prefetch_desc(&tma_b);
-        int64_t it = 0;
-        for (int64_t t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
-            const int64_t tm = t % tiles_m, tn = t / tiles_m;
-            const int64_t n0 = tn * BN;
-            const int nrt = (args.N - n0) >= 256 ? 2 : 1;   // 128-row scale tiles present in B
-            for (int64_t ks = 0; ks < kstages; ++ks, ++it) {
-                const int s = (int)(it % kStages);
-                if (it >= kStages && !mbar_wait(&ctl->empty[s], (uint32_t)(((it / kStages) - 1) & 1), ws, abort))
+        uint32_t s = 0, phase = 0, issued = 0;
+        for (uint32_t t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
+            const uint32_t tm = t % tiles_m, tn = t / tiles_m;
+            const int32_t m0 = (int32_t)(tm * BM), n0 = (int32_t)(tn * BN);
+            const uint32_t nrt = (args.N - n0) >= 256 ? 2u : 1u;  // 128-row scale tiles present in B
+            const uint8_t* sfa_t = args.sfa + (size_t)tm * cp * 512;
+            const uint8_t* sfb_t = args.sfb + (size_t)(2 * tn) * cp * 512;
+            for (uint32_t ks = 0; ks < kstages; ++ks) {
+                if (issued >= kStages && !mbar_wait(&ctl->empty[s], phase ^ 1, ws, abort))
                     goto producer_done;
                 uint8_t* st = smem + (size_t)s * kStageBytes;
-                const int64_t groups_left = cp - ks * 4;
-                const uint32_t gk = (uint32_t)(groups_left < 4 ? groups_left : 4);
-                const uint32_t bytes = kABytes + kBBytes + gk * 512u * (1u + (uint32_t)nrt);
-                mbar_expect_tx(&ctl->full[s], bytes);
-                tma_load_2d(st, &tma_a, &ctl->full[s], (int32_t)(ks * 128), (int32_t)(tm * BM));
-                tma_load_2d(st + kABytes, &tma_b, &ctl->full[s], (int32_t)(ks * 128), (int32_t)n0);
-                bulk_load(st + kABytes + kBBytes, args.sfa + (tm * cp + ks * 4) * 512, gk * 512u, &ctl->full[s]);
-                for (int h = 0; h < nrt; ++h)
-                    bulk_load(st + kABytes + kBBytes + kSfaBytes + h * 2048,
-                              args.sfb + ((2 * tn + h) * cp + ks * 4) * 512, gk * 512u, &ctl->full[s]);
+                const uint32_t left = cp - ks * 4;
+                const uint32_t gk = left < 4 ? left : 4;
+                mbar_expect_tx(&ctl->full[s], kABytes + kBBytes + gk * 512u * (1u + nrt));
+                tma_load_2d(st, &tma_a, &ctl->full[s], (int32_t)(ks * 128), m0);
+                tma_load_2d(st + kABytes, &tma_b, &ctl->full[s], (int32_t)(ks * 128), n0);
+                bulk_load(st + kABytes + kBBytes, sfa_t + ks * 2048, gk * 512u, &ctl->full[s]);
+                bulk_load(st + kABytes + kBBytes + kSfaBytes, sfb_t + ks * 2048, gk * 512u, &ctl->full[s]);
+                if (nrt == 2)
+                    bulk_load(st + kABytes + kBBytes + kSfaBytes + 2048, sfb_t + (size_t)cp * 512 + ks * 2048,
+                              gk * 512u, &ctl->full[s]);
+                ++issued;
+                if (++s == kStages) {
+                    s = 0;
+                    phase ^= 1;
+                }
             }
         }
     producer_done:
-        for (int64_t i = it > kStages ? it - kStages : 0; i < it; ++i)
-            mbar_wait(&ctl->full[i % kStages], (uint32_t)((i / kStages) & 1), ws, nullptr);
+        // never leave with copies in flight: wait for the last kStages loads
+        {
+            const uint32_t n = issued < kStages ? issued : kStages;
+            for (uint32_t i = 0; i < n; ++i) {
+                s = (s == 0) ? kStages - 1 : s - 1;
+                if (s == kStages - 1)
+                    phase ^= 1;
+                mbar_wait(&ctl->full[s], phase, ws, nullptr);
+            }
+        }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------ MMA issuer ----
-        int64_t it = 0, titer = 0;
-        for (int64_t t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++titer) {
-            if (titer > 0 && !mbar_wait(&ctl->tmem_empty, (uint32_t)((titer - 1) & 1), ws, abort))
+        const uint32_t base = smem_u32(smem);
+        const uint64_t a_desc = smem_desc(base, 16, 1024, kSwizzle128B);
+        const uint64_t b_desc = smem_desc(base + kABytes, 16, 1024, kSwizzle128B);
+        const uint64_t sfa_desc = smem_desc(base + kABytes + kBBytes, 0, 128, kSwizzleNone);
+        const uint64_t sfb_desc = smem_desc(base + kABytes + kBBytes + kSfaBytes, 0, 128, kSwizzleNone);
+        constexpr uint32_t kStageDesc = kStageBytes >> 4;  // stage stride in descriptor units
+        uint32_t s = 0, phase = 0, titer = 0;
+        for (uint32_t t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++titer) {
+            if (titer > 0 && !mbar_wait(&ctl->tmem_empty, (titer - 1) & 1, ws, abort))
                 break;
             tc_fence_after();
-            for (int64_t ks = 0; ks < kstages; ++ks, ++it) {
-                const int s = (int)(it % kStages);
-                if (!mbar_wait(&ctl->full[s], (uint32_t)((it / kStages) & 1), ws, abort))
+            for (uint32_t ks = 0; ks < kstages; ++ks) {
+                if (!mbar_wait(&ctl->full[s], phase, ws, abort))
                     goto mma_done;
                 tc_fence_after();
-                const uint32_t st = smem_u32(smem + (size_t)s * kStageBytes);
-                const int64_t k_left = args.K - ks * BK;
-                const int kk = (int)(k_left >= BK ? 4 : k_left / 64);
-                const uint32_t sf_col = kAccCols + (uint32_t)s * kSfColsPerStage;
-                for (int j = 0; j < kk; ++j) {
-                    const uint32_t sfa_s = st + kABytes + kBBytes + j * 512;
-                    const uint32_t sfb_s = st + kABytes + kBBytes + kSfaBytes + j * 512;
-                    tmem_cp_32x128b_x4(tmem + sf_col + 4 * j, smem_desc(sfa_s, 0, 128, kSwizzleNone));
-                    tmem_cp_32x128b_x4(tmem + sf_col + 16 + 8 * j, smem_desc(sfb_s, 0, 128, kSwizzleNone));
-                    tmem_cp_32x128b_x4(tmem + sf_col + 16 + 8 * j + 4, smem_desc(sfb_s + 2048, 0, 128, kSwizzleNone));
-                }
-                for (int j = 0; j < kk; ++j) {
-                    const uint64_t ad = smem_desc(st + 32 * j, 16, 1024, kSwizzle128B);
-                    const uint64_t bd = smem_desc(st + kABytes + 32 * j, 16, 1024, kSwizzle128B);
-                    mma_nvf4(tmem, ad, bd, kIdesc, tmem + sf_col + 4 * j, tmem + sf_col + 16 + 8 * j,
-                             (ks > 0 || j > 0) ? 1u : 0u);
+                const uint64_t off = (uint64_t)(s * kStageDesc);
+                const uint32_t sfa_t = tmem + kAccCols + s * kSfColsPerStage;
+                const uint32_t sfb_t = sfa_t + 16;
+                const uint32_t k_left = (uint32_t)args.K - ks * BK;
+                if (k_left >= BK) {
+#pragma unroll
+                    for (uint32_t j = 0; j < 4; ++j) {
+                        tmem_cp_32x128b_x4(sfa_t + 4 * j, sfa_desc + off + 32 * j);
+                        tmem_cp_32x128b_x4(sfb_t + 8 * j, sfb_desc + off + 32 * j);
+                        tmem_cp_32x128b_x4(sfb_t + 8 * j + 4, sfb_desc + off + 128 + 32 * j);
+                    }
+#pragma unroll
+                    for (uint32_t j = 0; j < 4; ++j)
+                        mma_nvf4(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, kIdesc, sfa_t + 4 * j,
+                                 sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                } else {
+                    const uint32_t kk = k_left / 64;
+                    for (uint32_t j = 0; j < kk; ++j) {
+                        tmem_cp_32x128b_x4(sfa_t + 4 * j, sfa_desc + off + 32 * j);
+                        tmem_cp_32x128b_x4(sfb_t + 8 * j, sfb_desc + off + 32 * j);
+                        tmem_cp_32x128b_x4(sfb_t + 8 * j + 4, sfb_desc + off + 128 + 32 * j);
+                    }
+                    for (uint32_t j = 0; j < kk; ++j)
+                        mma_nvf4(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, kIdesc, sfa_t + 4 * j,
+                                 sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
                 }
                 tc_commit(&ctl->empty[s]);
+                if (++s == kStages) {
+                    s = 0;
+                    phase ^= 1;
+                }
             }
             tc_commit(&ctl->tmem_full);
         }
@@ -174,71 +216,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&ctl->drain, 0, ws, nullptr);
     } else if (warp >= 2) {
         // -------------------------------------------------------- epilogue ----
-        const int q = warp & 3;                      // tensor-memory lane quarter
+        const uint32_t q = warp & 3;             // tensor-memory lane quarter of this warp
+        const uint32_t half = (warp - 2) >> 2;   // columns 128*half .. +127
         const float alpha = __fmul_rn(*args.ga, *args.gb);
-        int64_t titer = 0;
-        for (int64_t t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++titer) {
-            const int64_t tm = t % tiles_m, tn = t / tiles_m;
-            if (!mbar_wait(&ctl->tmem_full, (uint32_t)(titer & 1), ws, abort))
+        uint32_t titer = 0;
+        for (uint32_t t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++titer) {
+            const uint32_t tm = t % tiles_m, tn = t / tiles_m;
+            if (!mbar_wait(&ctl->tmem_full, titer & 1, ws, abort))
                 break;
             tc_fence_after();
-            const int64_t row = tm * BM + q * 32 + lane;
-            const int64_t n0 = tn * BN;
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-            if (args.out_f32) {
-                float* drow = reinterpret_cast<float*>(args.d) + row * args.ldd + n0;
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + c * 32, r);
-                    tmem_ld_wait();
-                    if (n0 + c * 32 < args.N) {
+            const int64_t row = (int64_t)tm * BM + q * 32 + lane;
+            const int32_t c0 = (int32_t)(tn * BN + half * 128);
+            const uint32_t taddr = tmem + ((q * 32) << 16) + half * 128;
+            uint32_t r[4][32];
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            reinterpret_cast<float4*>(drow + c * 32)[v] =
-                                make_float4(__fmul_rn(__uint_as_float(r[4 * v]), alpha),
-                                            __fmul_rn(__uint_as_float(r[4 * v + 1]), alpha),
-                                            __fmul_rn(__uint_as_float(r[4 * v + 2]), alpha),
-                                            __fmul_rn(__uint_as_float(r[4 * v + 3]), alpha));
+            for (int c = 0; c < 4; ++c)
+                tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+            tmem_ld_wait();
+            // the accumulator is free once every load has landed in registers
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ctl->tmem_empty);
+            if (c0 >= args.N)
+                continue;
+            uint8_t* buf = store_buf + (warp - 2) * kStoreBufBytes;
+            const int32_t row0 = (int32_t)(tm * BM + q * 32);
+            if (args.out_f32) {
+                // 16 chunks of 8 columns (32 bytes per row)
+#pragma unroll
+                for (int ch = 0; ch < 16; ++ch) {
+                    const uint32_t* rr = &r[ch >> 2][(ch & 3) * 8];
+                    uint32_t w[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        w[e] = __float_as_uint(__fmul_rn(__uint_as_float(rr[e]), alpha));
+                    if (lane == 0)
+                        bulk_wait_read0();
+                    __syncwarp();
+                    reinterpret_cast<uint4*>(buf + lane * 32)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    reinterpret_cast<uint4*>(buf + lane * 32)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tma_d, buf, c0 + ch * 8, row0);
+                        bulk_commit_group();
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&ctl->tmem_empty);
             } else {
-                uint32_t packed[BN / 2];
+                // 8 chunks of 16 columns (32 bytes per row)
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + c * 32, r);
-                    tmem_ld_wait();
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint32_t* rr = &r[ch >> 1][(ch & 1) * 16];
+                    uint32_t w[8];
 #pragma unroll
-                    for (int v = 0; v < 16; ++v)
-                        packed[c * 16 + v] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * v]), alpha),
-                                                         __fmul_rn(__uint_as_float(r[2 * v + 1]), alpha));
-                }
-                // accumulator is free once every load has landed in registers
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&ctl->tmem_empty);
-                __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(args.d) + row * args.ldd + n0;
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    if (n0 + c * 32 < args.N) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            reinterpret_cast<uint4*>(drow + c * 32)[v] =
-                                make_uint4(packed[c * 16 + 4 * v], packed[c * 16 + 4 * v + 1],
-                                           packed[c * 16 + 4 * v + 2], packed[c * 16 + 4 * v + 3]);
+                    for (int e = 0; e < 8; ++e)
+                        w[e] = pack_bf16x2(__fmul_rn(__uint_as_float(rr[2 * e]), alpha),
+                                           __fmul_rn(__uint_as_float(rr[2 * e + 1]), alpha));
+                    if (lane == 0)
+                        bulk_wait_read0();
+                    __syncwarp();
+                    reinterpret_cast<uint4*>(buf + lane * 32)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    reinterpret_cast<uint4*>(buf + lane * 32)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tma_d, buf, c0 + ch * 16, row0);
+                        bulk_commit_group();
                     }
                 }
             }
         }
+        if (lane == 0)
+            bulk_wait_all();
     }
 
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -258,6 +313,12 @@ nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, 
                               (uint64_t)N, (uint64_t)(K / 2), 128u, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return NVFP4_ERR_CUDA;
 
+    CUtensorMap md;
+    const bool f32 = dt == NVFP4_OUT_F32;
+    if (!encode_tensor_map_2d(&md, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d,
+                              (uint64_t)N, (uint64_t)M, (uint64_t)ldd * (f32 ? 4u : 2u), f32 ? 8u : 16u, 32u,
+                              CU_TENSOR_MAP_SWIZZLE_NONE))
+        return NVFP4_ERR_CUDA;
     static bool attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
@@ -268,11 +329,11 @@ nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, 
             return NVFP4_ERR_CUDA;
         attr_set[dev] = true;
     }
-    GemmArgs args{sfa, sfb, ga, gb, d, M, N, K, ldd, dt == NVFP4_OUT_F32 ? 1 : 0};
+    GemmArgs args{sfa, sfb, ga, gb, d, ldd, (int32_t)M, (int32_t)N, (int32_t)K, dt == NVFP4_OUT_F32 ? 1 : 0};
     const int64_t ntiles = (M / BM) * ((N + BN - 1) / BN);
     const int sms = device_sm_count();
     const int grid = (int)(ntiles < sms ? ntiles : sms);
-    nvf4_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, args, ws);
+    nvf4_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, md, args, ws);
     return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 

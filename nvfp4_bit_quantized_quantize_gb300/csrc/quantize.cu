@@ -32,7 +32,7 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;  // one 16-element block per consumer thread per tile
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // last warp is the TMA producer
 constexpr int kTileBytes = 16384;
@@ -42,6 +42,7 @@ struct SmemCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint32_t warp_amax[kConsumerWarps];
+    float ftab[128];  // ftab[b] = rn(s_enc / E4M3value(b)) for every non-zero scale byte b
     float amax;
     int abort;
 };
@@ -54,53 +55,48 @@ __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 1
 
 // --------------------------------------------------------- block quantize ----
 // Scale and round one block of 16 binary32 values.  Returns the scale byte;
-// writes 8 bytes of packed codes.
-__device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], float bamax, float s_enc, int mode,
-                                                  uint64_t seed, uint64_t blk, uint32_t& lo32, uint32_t& hi32)
+// writes 8 bytes of packed codes.  ftab holds rn(s_enc / E4M3value(b)) for the
+// 126 non-zero finite scale bytes: the same rounded quotient the definition
+// asks for, computed once per CTA instead of once per block.
+__device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], float bamax, float s_enc,
+                                                  const float* ftab, int mode, uint64_t seed, uint64_t blk,
+                                                  uint32_t& lo32, uint32_t& hi32)
 {
     const uint32_t sb = e4m3_rn_sat(__fmul_rn(__fdiv_rn(bamax, 6.0f), s_enc));
-    const float d = e4m3_value(sb);
-    uint32_t code[16];
-    if (d == 0.0f) {
+    if (sb == 0) {  // the block decodes to zero: signed zeros
+        lo32 = hi32 = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            lo32 |= ((__float_as_uint(x[j]) >> 28) & 8u) << (4 * j);
+            hi32 |= ((__float_as_uint(x[8 + j]) >> 28) & 8u) << (4 * j);
+        }
+        return 0;
+    }
+    const float f = ftab[sb];
+    float v[16];
+    if (isinf(f)) {
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            code[j] = (__float_as_uint(x[j]) >> 28) & 8u;
+            v[j] = (x[j] == 0.0f) ? x[j] : __fmul_rn(x[j], f);
     } else {
-        const float f = __fdiv_rn(s_enc, d);
-        float v[16];
-        if (isinf(f)) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                v[j] = (x[j] == 0.0f) ? x[j] : __fmul_rn(x[j], f);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                v[j] = __fmul_rn(x[j], f);
-        }
-        if (mode == NVFP4_ROUND_SR) {
-            const U4 w = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, (uint32_t)seed,
-                                       (uint32_t)(seed >> 32));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                code[j] = e2m1_sr(v[j], (ws[j >> 2] >> (8 * (j & 3))) & 0xFFu);
-        } else {
-            uint32_t bytes[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                bytes[j] = e2m1x2_rn(v[2 * j], v[2 * j + 1]);
-            lo32 = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
-            hi32 = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
-            return sb;
-        }
+        for (int j = 0; j < 16; ++j)
+            v[j] = __fmul_rn(x[j], f);
     }
-    lo32 = 0;
-    hi32 = 0;
+    if (mode == NVFP4_ROUND_SR) {
+        const U4 w = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, (uint32_t)seed,
+                                   (uint32_t)(seed >> 32));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        lo32 |= code[j] << (4 * j);
-        hi32 |= code[8 + j] << (4 * j);
+        for (int j = 0; j < 16; ++j)
+            v[j] = sr_grid_value(v[j], sr_threshold(ws[j >> 2], (uint32_t)(j & 3)));
     }
+    uint32_t bytes[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        bytes[j] = e2m1x2_rn(v[2 * j], v[2 * j + 1]);
+    lo32 = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+    hi32 = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
     return sb;
 }
 
@@ -119,23 +115,27 @@ __device__ __forceinline__ void tensor_scales(float amax, float& s_enc, float& g
     g = __fdiv_rn(amax, 2688.0f);
 }
 
-// Scan a 128 x 64 bf16 tile for max |x| (bf16x2 accumulator, NaN-propagating).
-__device__ __forceinline__ uint32_t scan_tile_bf16(const uint8_t* tile, int ctid, uint32_t acc)
+// Scan a 128 x 64 bf16 tile for max |x| (bf16x2 accumulator, NaN-propagating):
+// thread ctid reads block (row ctid / 4, block ctid % 4).
+__device__ __forceinline__ uint32_t scan_tile_bf16(const uint8_t* tile, int ctid)
 {
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const uint32_t row = (uint32_t)(ctid >> 2) + 64u * k, blk = ctid & 3;
-        const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
-        const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
-        acc = habs_max2(acc, a.x); acc = habs_max2(acc, a.y);
-        acc = habs_max2(acc, a.z); acc = habs_max2(acc, a.w);
-        acc = habs_max2(acc, b.x); acc = habs_max2(acc, b.y);
-        acc = habs_max2(acc, b.z); acc = habs_max2(acc, b.w);
-    }
+    const uint32_t row = (uint32_t)ctid >> 2, blk = ctid & 3;
+    const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
+    const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
+    uint32_t acc = habs_max2(0u, a.x);
+    acc = habs_max2(acc, a.y);
+    acc = habs_max2(acc, a.z);
+    acc = habs_max2(acc, a.w);
+    acc = habs_max2(acc, b.x);
+    acc = habs_max2(acc, b.y);
+    acc = habs_max2(acc, b.z);
+    acc = habs_max2(acc, b.w);
     return acc;
 }
 
 // ------------------------------------------------------------------ 1x16 ----
+// Consumer thread ctid owns block (row ctid / 4, block ctid % 4) of the tile;
+// the 4 blocks of a row sit in lanes 4i..4i+3 of one warp.
 struct Op1x16 {
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
                                  const QuantParams& p)
@@ -146,46 +146,40 @@ struct Op1x16 {
 
     __device__ static uint32_t phase1(const uint8_t* tile, int ctid, const QuantParams&)
     {
-        return hmax_to_float_bits(scan_tile_bf16(tile, ctid, 0u));
+        return __float_as_uint(hmax_to_float(scan_tile_bf16(tile, ctid)));
     }
 
-    __device__ static uint32_t hmax_to_float_bits(uint32_t acc) { return __float_as_uint(hmax_to_float(acc)); }
-
-    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const QuantParams& p)
+    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const float* ftab,
+                                  const QuantParams& p)
     {
         const int64_t tr = t / p.tiles_c, tc = t % p.tiles_c;
         const int lane = ctid & 31;
-        const int64_t kblocks = p.cols / 16;
-#pragma unroll 1
-        for (int k = 0; k < 2; ++k) {
-            const uint32_t row = (uint32_t)(ctid >> 2) + 64u * k, blk = ctid & 3;
-            const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
-            const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            float x[16];
-            uint32_t acc = 0;
+        const uint32_t row = (uint32_t)ctid >> 2, blk = ctid & 3;
+        const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
+        const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float x[16];
+        uint32_t acc = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                x[2 * j] = bf16lo(w[j]);
-                x[2 * j + 1] = bf16hi(w[j]);
-                acc = habs_max2(acc, w[j]);
-            }
-            const int64_t grow = tr * 128 + row;
-            const int64_t gcol = tc * 64 + blk * 16;
-            uint32_t lo32, hi32;
-            const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc, p.mode, p.sr_seed,
-                                              (uint64_t)(grow * kblocks + gcol / 16), lo32, hi32);
-            if (grow < p.rows && gcol < p.cols)
-                *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
-            // the 4 blocks of this row sit in lanes 4i..4i+3: one 4-byte store
-            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
-            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
-            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
-            if ((lane & 3) == 0) {
-                const int64_t atom = (tr * p.tiles_c + tc) * 512;
-                *reinterpret_cast<uint32_t*>(p.sf + atom + (row & 31) * 16 + (row >> 5) * 4) =
-                    sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
-            }
+        for (int j = 0; j < 8; ++j) {
+            x[2 * j] = bf16lo(w[j]);
+            x[2 * j + 1] = bf16hi(w[j]);
+            acc = habs_max2(acc, w[j]);
+        }
+        const int64_t grow = tr * 128 + row;
+        const int64_t gcol = tc * 64 + blk * 16;
+        uint32_t lo32, hi32;
+        const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc, ftab, p.mode, p.sr_seed,
+                                          (uint64_t)(grow * (p.cols / 16) + gcol / 16), lo32, hi32);
+        if (grow < p.rows && gcol < p.cols)
+            *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
+        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
+        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
+        if ((lane & 3) == 0) {
+            const int64_t atom = (tr * p.tiles_c + tc) * 512;
+            *reinterpret_cast<uint32_t*>(p.sf + atom + (row & 31) * 16 + (row >> 5) * 4) =
+                sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
         }
     }
 };
@@ -211,6 +205,8 @@ __device__ __forceinline__ uint64_t nibble_transpose16(uint64_t w, int i)
     return w;
 }
 
+// Each half-warp owns one 16 x 16 tile: lanes 0-15 tile 2w, lanes 16-31 tile
+// 2w + 1 of the 32 tiles (8 row groups x 4 column blocks); lane i has row i.
 struct Op2d {
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
                                  const QuantParams& p)
@@ -223,56 +219,54 @@ struct Op2d {
         return Op1x16::phase1(tile, ctid, p);
     }
 
-    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const QuantParams& p)
+    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const float* ftab,
+                                  const QuantParams& p)
     {
         const int64_t tr = t / p.tiles_c, tc = t % p.tiles_c;
         const int lane = ctid & 31, cw = ctid >> 5;
         const int64_t kblocksT = p.rows / 16;
         const int64_t cpT = (kblocksT + 3) / 4;
-#pragma unroll 1
-        for (int k = 0; k < 2; ++k) {
-            const int P = k * 16 + cw * 2 + (lane >> 4);
-            const uint32_t g = P >> 2, blk = P & 3, i = lane & 15;
-            const uint32_t row = g * 16 + i;
-            const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
-            const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            float x[16];
-            uint32_t acc = 0;
+        const int P = cw * 2 + (lane >> 4);
+        const uint32_t g = P >> 2, blk = P & 3, i = lane & 15;
+        const uint32_t row = g * 16 + i;
+        const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
+        const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float x[16];
+        uint32_t acc = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                x[2 * j] = bf16lo(w[j]);
-                x[2 * j + 1] = bf16hi(w[j]);
-                acc = habs_max2(acc, w[j]);
-            }
-            uint32_t m = __float_as_uint(hmax_to_float(acc));
+        for (int j = 0; j < 8; ++j) {
+            x[2 * j] = bf16lo(w[j]);
+            x[2 * j + 1] = bf16hi(w[j]);
+            acc = habs_max2(acc, w[j]);
+        }
+        uint32_t m = __float_as_uint(hmax_to_float(acc));
 #pragma unroll
-            for (int off = 1; off < 16; off <<= 1)
-                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-            const int64_t grow = tr * 128 + row;
-            const int64_t gcol = tc * 64 + blk * 16;
-            uint32_t lo32, hi32;
-            const uint32_t sb = quant_block16(x, __uint_as_float(m), s_enc, NVFP4_ROUND_RN, 0, 0, lo32, hi32);
-            if (grow < p.rows && gcol < p.cols)
-                *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
-            p.sf[(tr * p.tiles_c + tc) * 512 + (row & 31) * 16 + (row >> 5) * 4 + blk] = (uint8_t)sb;
-            if (p.qT != nullptr) {
-                const uint64_t col = nibble_transpose16(((uint64_t)hi32 << 32) | lo32, (int)i);
-                const int64_t rT = gcol + i;          // row of the transposed matrix
-                const int64_t kbT = tr * 8 + g;       // its 16-block index
-                if (rT < p.cols && kbT < kblocksT)
-                    *reinterpret_cast<uint2*>(p.qT + rT * (p.rows / 2) + kbT * 8) =
-                        make_uint2((uint32_t)col, (uint32_t)(col >> 32));
-                if (kbT < 4 * cpT) {
-                    p.sfT[((rT >> 7) * cpT + (kbT >> 2)) * 512 + (rT & 31) * 16 + ((rT & 127) >> 5) * 4 +
-                          (kbT & 3)] = (uint8_t)sb;
-                    // an odd count of 64-column tiles leaves the upper half of
-                    // the last 128-row scale atom to padding: write its zeros
-                    if ((p.tiles_c & 1) && tc == p.tiles_c - 1) {
-                        const int64_t rP = rT + 64;
-                        p.sfT[((rP >> 7) * cpT + (kbT >> 2)) * 512 + (rP & 31) * 16 + ((rP & 127) >> 5) * 4 +
-                              (kbT & 3)] = 0;
-                    }
+        for (int off = 1; off < 16; off <<= 1)
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+        const int64_t grow = tr * 128 + row;
+        const int64_t gcol = tc * 64 + blk * 16;
+        uint32_t lo32, hi32;
+        const uint32_t sb = quant_block16(x, __uint_as_float(m), s_enc, ftab, NVFP4_ROUND_RN, 0, 0, lo32, hi32);
+        if (grow < p.rows && gcol < p.cols)
+            *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
+        p.sf[(tr * p.tiles_c + tc) * 512 + (row & 31) * 16 + (row >> 5) * 4 + blk] = (uint8_t)sb;
+        if (p.qT != nullptr) {
+            const uint64_t col = nibble_transpose16(((uint64_t)hi32 << 32) | lo32, (int)i);
+            const int64_t rT = gcol + i;     // row of the transposed matrix
+            const int64_t kbT = tr * 8 + g;  // its 16-block index
+            if (rT < p.cols && kbT < kblocksT)
+                *reinterpret_cast<uint2*>(p.qT + rT * (p.rows / 2) + kbT * 8) =
+                    make_uint2((uint32_t)col, (uint32_t)(col >> 32));
+            if (kbT < 4 * cpT) {
+                p.sfT[((rT >> 7) * cpT + (kbT >> 2)) * 512 + (rT & 31) * 16 + ((rT & 127) >> 5) * 4 + (kbT & 3)] =
+                    (uint8_t)sb;
+                // an odd count of 64-column tiles leaves the upper half of
+                // the last 128-row scale atom to padding: write its zeros
+                if ((p.tiles_c & 1) && tc == p.tiles_c - 1) {
+                    const int64_t rP = rT + 64;
+                    p.sfT[((rP >> 7) * cpT + (kbT >> 2)) * 512 + (rP & 31) * 16 + ((rP & 127) >> 5) * 4 +
+                          (kbT & 3)] = 0;
                 }
             }
         }
@@ -280,8 +274,10 @@ struct Op2d {
 };
 
 // ------------------------------------------------------------------- RHT ----
+// Tile = 64 tokens x 128 channels as two 64 x 64 boxes (8 KB each).  Consumer
+// warp w handles token block tb = w / 4 and channels 32 (w % 4) .. + 31, one
+// channel per lane, 16 tokens per thread.
 struct OpRht {
-    // tile = 64 tokens x 128 channels as two 64 x 64 boxes (8 KB each)
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
                                  const QuantParams& p)
     {
@@ -290,21 +286,18 @@ struct OpRht {
         tma_load_2d(dst + 8192, m, bar, (int32_t)(ct * 128 + 64), (int32_t)(tt * 64));
     }
 
-    // y = (1/4) H16 D v for the two channels held by this thread.
-    __device__ static void transform(const uint8_t* tile, int ctid, uint32_t signs, float (&y0)[16],
-                                     float (&y1)[16])
+    // y = (1/4) H16 D v for this thread's channel and token block.
+    __device__ static void transform(const uint8_t* tile, int ctid, uint32_t signs, float (&y)[16])
     {
         const int lane = ctid & 31, cw = ctid >> 5;
-        const uint32_t tb = cw >> 1, h = cw & 1;
-        const uint8_t* half = tile + h * 8192;
+        const uint32_t tb = cw >> 2, cl = (cw & 3) * 32 + lane;
+        const uint8_t* half = tile + (cl >> 6) * 8192;
+        const uint32_t cb = cl & 63;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint32_t row = tb * 16 + i;
-            const uint32_t w =
-                *reinterpret_cast<const uint32_t*>(half + sw128(row, (uint32_t)lane >> 2) + (lane & 3) * 4);
-            const uint32_t flip = ((signs >> i) & 1u) << 31;
-            y0[i] = __uint_as_float((w << 16) ^ flip);
-            y1[i] = __uint_as_float((w & 0xFFFF0000u) ^ flip);
+            const uint32_t h = *reinterpret_cast<const uint16_t*>(half + sw128(row, cb >> 3) + (cb & 7) * 2);
+            y[i] = __uint_as_float((h << 16) ^ (((signs >> i) & 1u) << 31));
         }
 #pragma unroll
         for (int hs = 1; hs < 16; hs <<= 1) {
@@ -312,60 +305,50 @@ struct OpRht {
             for (int i = 0; i < 16; ++i) {
                 if (i & hs)
                     continue;
-                const float a0 = y0[i], b0 = y0[i + hs];
-                y0[i] = __fadd_rn(a0, b0);
-                y0[i + hs] = __fsub_rn(a0, b0);
-                const float a1 = y1[i], b1 = y1[i + hs];
-                y1[i] = __fadd_rn(a1, b1);
-                y1[i + hs] = __fsub_rn(a1, b1);
+                const float a = y[i], b = y[i + hs];
+                y[i] = __fadd_rn(a, b);
+                y[i + hs] = __fsub_rn(a, b);
             }
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            y0[i] = __fmul_rn(y0[i], 0.25f);
-            y1[i] = __fmul_rn(y1[i], 0.25f);
-        }
+        for (int i = 0; i < 16; ++i)
+            y[i] = __fmul_rn(y[i], 0.25f);
     }
 
     __device__ static uint32_t phase1(const uint8_t* tile, int ctid, const QuantParams& p)
     {
-        float y0[16], y1[16];
-        transform(tile, ctid, p.rht_signs, y0, y1);
+        float y[16];
+        transform(tile, ctid, p.rht_signs, y);
         uint32_t m = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            m = max(m, __float_as_uint(y0[i]) & 0x7FFFFFFFu);
-            m = max(m, __float_as_uint(y1[i]) & 0x7FFFFFFFu);
-        }
+        for (int i = 0; i < 16; ++i)
+            m = max(m, __float_as_uint(y[i]) & 0x7FFFFFFFu);
         return m;
     }
 
-    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const QuantParams& p)
+    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const float* ftab,
+                                  const QuantParams& p)
     {
         const int64_t tt = t / p.tiles_c, ct = t % p.tiles_c;
         const int lane = ctid & 31, cw = ctid >> 5;
-        const uint32_t tb = cw >> 1, h = cw & 1;
+        const uint32_t tb = cw >> 2, cl = (cw & 3) * 32 + lane;
         const int64_t T = p.rows, C = p.cols;
         const int64_t kblocks = T / 16;
         const int64_t cp = (kblocks + 3) / 4;
-        float y[2][16];
-        transform(tile, ctid, p.rht_signs, y[0], y[1]);
+        float y[16];
+        transform(tile, ctid, p.rht_signs, y);
+        float bamax = 0.0f;
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-            float bamax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                bamax = fmaxf(bamax, fabsf(y[ch][i]));
-            const uint32_t cl = h * 64 + 2 * lane + ch;  // channel within tile
-            const int64_t c = ct * 128 + cl;
-            const int64_t kb = tt * 4 + tb;
-            uint32_t lo32, hi32;
-            const uint32_t sb =
-                quant_block16(y[ch], bamax, s_enc, p.mode, p.sr_seed, (uint64_t)(c * kblocks + kb), lo32, hi32);
-            if (c < C && kb < kblocks)
-                *reinterpret_cast<uint2*>(p.q + c * (T / 2) + kb * 8) = make_uint2(lo32, hi32);
-            p.sf[(ct * cp + tt) * 512 + (cl & 31) * 16 + (cl >> 5) * 4 + tb] = (uint8_t)sb;
-        }
+        for (int i = 0; i < 16; ++i)
+            bamax = fmaxf(bamax, fabsf(y[i]));
+        const int64_t c = ct * 128 + cl;
+        const int64_t kb = tt * 4 + tb;
+        uint32_t lo32, hi32;
+        const uint32_t sb =
+            quant_block16(y, bamax, s_enc, ftab, p.mode, p.sr_seed, (uint64_t)(c * kblocks + kb), lo32, hi32);
+        if (c < C && kb < kblocks)
+            *reinterpret_cast<uint2*>(p.q + c * (T / 2) + kb * 8) = make_uint2(lo32, hi32);
+        p.sf[(ct * cp + tt) * 512 + (cl & 31) * 16 + (cl >> 5) * 4 + tb] = (uint8_t)sb;
     }
 };
 
@@ -463,6 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tensor_scales(ctl->amax, s_enc, g);
     if (bid == 0 && ctid == 0)
         *p.g_dec = g;
+    if (ctid < 128)
+        ctl->ftab[ctid] = (ctid == 0 || ctid == 127) ? 0.0f : __fdiv_rn(s_enc, e4m3_value((uint32_t)ctid));
+    named_bar_sync(1, kConsumers);
 
     volatile int* abort_flag = &ctl->abort;
     for (int64_t j = 0; j < n && !*abort_flag; ++j) {
@@ -471,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= R && !mbar_wait(&ctl->full[s], (uint32_t)((i / stages) & 1), ws, &ctl->abort))
             break;
         const int64_t tile = (j < R) ? t_begin + n - R + j : t_begin + (n - R - 1) - (j - R);
-        Op::phase2(smem + (size_t)s * kTileBytes, tile, ctid, s_enc, p);
+        Op::phase2(smem + (size_t)s * kTileBytes, tile, ctid, s_enc, ctl->ftab, p);
         __syncwarp();
         if (lane == 0)
             mbar_arrive(&ctl->empty[s]);
