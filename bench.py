@@ -2,14 +2,18 @@
 """NVFP4 linear-layer benchmark on one GB300 (or N independent replicas).
 
 One step = the whole NVFP4 hot path of a 7B-shape MLP (hidden 4096, FFN 11008,
-8192 tokens, no activation function) forward and backward, 16 kernel launches:
+8192 tokens, no activation function) forward and backward, 12 kernel launches:
 
-  quantize(X, RN) . quantize_2d(W_up, +T) . GEMM  H  = X W_up^T
-  quantize(H, RN) . quantize_2d(W_down, +T) . GEMM  Y  = H W_down^T
-  quantize(dY, SR) . GEMM dH = dY W_down                     (Dgrad down)
-  rht_quantize(dY, SR) . rht_quantize(H, RN) . GEMM dW_down = dY^T H (Wgrad)
-  quantize(dH, SR) . GEMM dX = dH W_up                       (Dgrad up)
-  rht_quantize(dH, SR) . rht_quantize(X, RN) . GEMM dW_up = dH^T X  (Wgrad)
+  dual(X: RN | RHT RN) . quantize_2d(W_up, +T) . GEMM  H  = X W_up^T
+  dual(H: RN | RHT RN) . quantize_2d(W_down, +T) . GEMM  Y  = H W_down^T
+  dual(dY: SR | RHT SR) . GEMM dH = dY W_down                (Dgrad down)
+                          GEMM dW_down = dY^T H              (Wgrad down)
+  dual(dH: SR | RHT SR) . GEMM dX = dH W_up                  (Dgrad up)
+                          GEMM dW_up = dH^T X                (Wgrad up)
+
+dual(.) is one read of a bf16 tensor that writes both its 1x16 row form (for
+the Fprop/Dgrad GEMMs) and its Hadamard-transformed, transposed form (for the
+Wgrad GEMMs), each bit-identical to the single-form quantizers.
 
 Six GEMMs of 2*8192*11008*4096 flops.  `value` is NVFP4 TFLOP/s of the whole
 step (all quantizers included) with inputs resident in HBM; `e2e` is the same
@@ -62,7 +66,7 @@ def quant_bytes(kind: str, rows: int, cols: int) -> float:
     n = rows * cols
     reads = 1 if 2 * n <= 0.5 * L2_BYTES else 2
     out = n / 2 + n / 16
-    if kind == "quantize_2d_t":
+    if kind in ("quantize_2d_t", "quantize_dual"):
         out *= 2
     return reads * 2.0 * n + out
 
@@ -145,7 +149,7 @@ class ClockSampler:
 # --------------------------------------------------------------- our arm ----
 
 class MlpStep:
-    """Device buffers and the 16 launches of one fwd+bwd step.
+    """Device buffers and the 12 launches of one fwd+bwd step.
 
     Inputs (X, W_up, W_down, dY_down) and results (Y, dX, dW_up, dW_down) have
     two device slots, so that the end-to-end leg can copy the next step's
@@ -192,31 +196,29 @@ class MlpStep:
         T, D, F = TOKENS, HIDDEN, FFN
         ws, s = self.ws, self.seed
         rht_seed = s + 1
-        Q = nv.nvfp4_quantize
         Q2 = nv.nvfp4_quantize_2d
-        R = nv.nvfp4_rht_quantize
+        QD = nv.nvfp4_quantize_dual
 
         def G(a, b, d, M, N, K):
             return lambda: nv.nvfp4_gemm(a[0], a[1], a[2], b[0], b[1], b[2], M, N, K, d, N, nv.OUT_BF16, ws)
 
+        def dual(x, C, rows_q, t_q, mode, seed, seed_t):
+            return lambda: QD(x, T, C, C, mode, seed, *rows_q, rht_seed, mode, seed_t, *t_q, ws)
+
         return [
-            ("quantize_1x16", ("rn", T, D), lambda: Q(x, T, D, D, nv.RN, 0, *self.xq, ws)),
+            ("quantize_dual", ("rn", T, D), dual(x, D, self.xq, self.xT, nv.RN, 0, 0)),
             ("quantize_2d_t", ("rn", F, D), lambda: Q2(wu, F, D, D, self.wuq[0], self.wuq[1], self.wuqT[0],
                                                        self.wuqT[1], self.wuq[2], ws)),
             ("gemm", (T, F, D), G(self.xq, self.wuq, self.H, T, F, D)),
-            ("quantize_1x16", ("rn", T, F), lambda: Q(self.H, T, F, F, nv.RN, 0, *self.hq, ws)),
+            ("quantize_dual", ("rn", T, F), dual(self.H, F, self.hq, self.hT, nv.RN, 0, 0)),
             ("quantize_2d_t", ("rn", D, F), lambda: Q2(wd, D, F, F, self.wdq[0], self.wdq[1], self.wdqT[0],
                                                        self.wdqT[1], self.wdq[2], ws)),
             ("gemm", (T, D, F), G(self.hq, self.wdq, Y, T, D, F)),
-            ("quantize_1x16", ("sr", T, D), lambda: Q(dy, T, D, D, nv.SR, s * 16 + 3, *self.dyq, ws)),
+            ("quantize_dual", ("sr", T, D), dual(dy, D, self.dyq, self.dyT, nv.SR, s * 16 + 3, s * 16 + 4)),
             ("gemm", (T, F, D), G(self.dyq, (self.wdqT[0], self.wdqT[1], self.wdq[2]), self.dH, T, F, D)),
-            ("rht_quantize", ("sr", T, D), lambda: R(dy, T, D, D, rht_seed, nv.SR, s * 16 + 4, *self.dyT, ws)),
-            ("rht_quantize", ("rn", T, F), lambda: R(self.H, T, F, F, rht_seed, nv.RN, 0, *self.hT, ws)),
             ("gemm", (D, F, T), G(self.dyT, self.hT, dW_down, D, F, T)),
-            ("quantize_1x16", ("sr", T, F), lambda: Q(self.dH, T, F, F, nv.SR, s * 16 + 5, *self.dhq, ws)),
+            ("quantize_dual", ("sr", T, F), dual(self.dH, F, self.dhq, self.dhT, nv.SR, s * 16 + 5, s * 16 + 6)),
             ("gemm", (T, D, F), G(self.dhq, (self.wuqT[0], self.wuqT[1], self.wuq[2]), dX, T, D, F)),
-            ("rht_quantize", ("sr", T, F), lambda: R(self.dH, T, F, F, rht_seed, nv.SR, s * 16 + 6, *self.dhT, ws)),
-            ("rht_quantize", ("rn", T, D), lambda: R(x, T, D, D, rht_seed, nv.RN, 0, *self.xT, ws)),
             ("gemm", (F, D, T), G(self.dhT, self.xT, dW_up, F, D, T)),
         ]
 
@@ -459,7 +461,8 @@ def oracle_step_estimate(budget_s: float):
     total = quant + t_mac * (N_GEMMS * GEMM_FLOPS / 2)
     sample = (f"oracle timed on {r_rn}x{D} (1x16 RN), {r_sr}x{D} (1x16 SR), {16 * r_2d}x{D} (2-D), "
               f"{T}x{8 * c_rht} (RHT+SR) slices and {n_out} GEMM outputs at K={K}; per-element and "
-              f"per-MAC times extrapolated to the full step ({N_GEMMS} GEMMs, 10 quantizer launches)")
+              f"per-MAC times extrapolated to the full step ({N_GEMMS} GEMMs; the 1x16, Hadamard and "
+              f"2-D quantizations of the step's 4 dual and 2 weight launches)")
     return total, sample
 
 

@@ -139,6 +139,26 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t T, int64_t C, int64_t ld,
                                 void* ws, nvfp4_stream_t stream);
 
 /*
+ * Both quantized forms of one activation or gradient x [T, C] from a single
+ * read of x: the 1x16 row form (q, sf, g_dec; exactly what nvfp4_quantize
+ * writes with mode / sr_seed) for the forward or data-gradient matmul, and
+ * the Hadamard-transformed transposed form (qT, sfT, g_dec_t; exactly what
+ * nvfp4_rht_quantize writes with rht_seed / mode_t / sr_seed_t) for the
+ * weight-gradient matmul ["Entrenamiento ...", "Metodología de
+ * Entrenamiento": each matmul's operands are quantized along its reduction
+ * dimension; random Hadamard transforms on Wgrad inputs].  Each form has its
+ * own tensor amax and decode scale.  T % 16 == 0, C % 16 == 0.  All outputs
+ * are device buffers owned by the caller; the errors are those of the two
+ * single-form calls.
+ */
+nvfp4_status nvfp4_quantize_dual(const void* x, int64_t T, int64_t C, int64_t ld,
+                                 nvfp4_round mode, uint64_t sr_seed,
+                                 uint8_t* q, uint8_t* sf, float* g_dec,
+                                 uint64_t rht_seed, nvfp4_round mode_t, uint64_t sr_seed_t,
+                                 uint8_t* qT, uint8_t* sfT, float* g_dec_t,
+                                 void* ws, nvfp4_stream_t stream);
+
+/*
  * Block-scaled NVFP4 matmul on the tcgen05 tensor cores [NVFP4 is supported
  * by Blackwell tensor cores: "Entrenamiento ...", "El Desafío de la
  * Precisión de 4 Bits"].

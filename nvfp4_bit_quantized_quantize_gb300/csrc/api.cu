@@ -98,6 +98,28 @@ nvfp4_status check_device()
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// The random sign diagonal of the 16-point Hadamard transform: bit i of word 0
+// of Philox4x32-10 (key = rht_seed, counter = (0, 0, 1, 0)) flips the sign of
+// input i.
+uint32_t rht_sign_bits(uint64_t rht_seed)
+{
+    uint32_t c[4] = {0u, 0u, 1u, 0u};
+    uint32_t k[2] = {(uint32_t)rht_seed, (uint32_t)(rht_seed >> 32)};
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k[0];
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k[1];
+        c[0] = n0;
+        c[1] = (uint32_t)p1;
+        c[2] = n2;
+        c[3] = (uint32_t)p0;
+        k[0] += 0x9E3779B9u;
+        k[1] += 0xBB67AE85u;
+    }
+    return c[0] & 0xFFFFu;
+}
+
 }  // namespace
 
 extern "C" {
@@ -135,7 +157,8 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
     p.rows = rows;
     p.cols = cols;
     p.tiles_c = cdiv(cols, 64);
-    p.ntiles = cdiv(rows, 128) * p.tiles_c;
+    p.tiles_r = cdiv(rows, 128);
+    p.ntiles = p.tiles_r * p.tiles_c;
     p.q = q;
     p.sf = sf;
     p.g_dec = g_dec;
@@ -162,7 +185,8 @@ nvfp4_status nvfp4_quantize_2d(const void* w, int64_t rows, int64_t cols, int64_
     p.rows = rows;
     p.cols = cols;
     p.tiles_c = cdiv(cols, 64);
-    p.ntiles = cdiv(rows, 128) * p.tiles_c;
+    p.tiles_r = cdiv(rows, 128);
+    p.ntiles = p.tiles_r * p.tiles_c;
     p.q = q;
     p.sf = sf;
     p.qT = qT;
@@ -185,33 +209,55 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t T, int64_t C, int64_t ld,
     nvfp4_status st = check_device();
     if (st != NVFP4_OK)
         return st;
-    // sign diagonal: bit i of word 0 of Philox(key = rht_seed, counter = (0, 0, 1, 0))
-    uint32_t c[4] = {0u, 0u, 1u, 0u};
-    uint32_t k[2] = {(uint32_t)rht_seed, (uint32_t)(rht_seed >> 32)};
-    for (int round = 0; round < 10; ++round) {
-        const uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
-        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
-        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k[0];
-        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k[1];
-        c[0] = n0;
-        c[1] = (uint32_t)p1;
-        c[2] = n2;
-        c[3] = (uint32_t)p0;
-        k[0] += 0x9E3779B9u;
-        k[1] += 0xBB67AE85u;
-    }
     QuantParams p = {};
     p.rows = T;
     p.cols = C;
     p.tiles_c = cdiv(C, 128);
-    p.ntiles = cdiv(T, 64) * p.tiles_c;
+    p.tiles_r = cdiv(T, 64);
+    p.ntiles = p.tiles_r * p.tiles_c;
     p.q = qT;
     p.sf = sfT;
     p.g_dec = g_dec;
     p.sr_seed = sr_seed;
-    p.rht_signs = c[0] & 0xFFFFu;
+    p.rht_signs = rht_sign_bits(rht_seed);
     p.mode = mode;
     return launch_quantize(QuantKind::kRht, x, ld, p, static_cast<Workspace*>(ws), (cudaStream_t)stream);
+}
+
+nvfp4_status nvfp4_quantize_dual(const void* x, int64_t T, int64_t C, int64_t ld, nvfp4_round mode,
+                                 uint64_t sr_seed, uint8_t* q, uint8_t* sf, float* g_dec, uint64_t rht_seed,
+                                 nvfp4_round mode_t, uint64_t sr_seed_t, uint8_t* qT, uint8_t* sfT, float* g_dec_t,
+                                 void* ws, nvfp4_stream_t stream)
+{
+    if (!x || !q || !sf || !g_dec || !qT || !sfT || !g_dec_t || !ws ||
+        (mode != NVFP4_ROUND_RN && mode != NVFP4_ROUND_SR) || (mode_t != NVFP4_ROUND_RN && mode_t != NVFP4_ROUND_SR))
+        return NVFP4_ERR_ARG;
+    if (T <= 0 || C <= 0 || T % 16 != 0 || C % 16 != 0 || ld < C || T > (1ll << 31) || C > (1ll << 31))
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sf) || !aligned16(qT) || !aligned16(sfT) || !aligned16(ws) ||
+        ld % 8 != 0)
+        return NVFP4_ERR_ALIGN;
+    nvfp4_status st = check_device();
+    if (st != NVFP4_OK)
+        return st;
+    QuantParams p = {};
+    p.rows = T;
+    p.cols = C;
+    p.tiles_c = cdiv(C, 128);
+    p.tiles_r = cdiv(T, 64);
+    p.ntiles = p.tiles_r * p.tiles_c;
+    p.q = q;
+    p.sf = sf;
+    p.g_dec = g_dec;
+    p.sr_seed = sr_seed;
+    p.mode = mode;
+    p.q2 = qT;
+    p.sf2 = sfT;
+    p.g_dec2 = g_dec_t;
+    p.sr_seed2 = sr_seed_t;
+    p.mode2 = mode_t;
+    p.rht_signs = rht_sign_bits(rht_seed);
+    return launch_quantize(QuantKind::kDual, x, ld, p, static_cast<Workspace*>(ws), (cudaStream_t)stream);
 }
 
 nvfp4_status nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,

@@ -225,7 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&ctl->tmem_full, titer & 1, ws, abort))
                 break;
             tc_fence_after();
-            const int64_t row = (int64_t)tm * BM + q * 32 + lane;
             const int32_t c0 = (int32_t)(tn * BN + half * 128);
             const uint32_t taddr = tmem + ((q * 32) << 16) + half * 128;
             uint32_t r[4][32];

@@ -16,7 +16,8 @@ struct Workspace {
     uint32_t amax_bits;   // max |x| over the tensor, as float bits (atomicMax)
     uint32_t arrived;     // CTAs that reached the grid barrier
     uint32_t departed;    // CTAs that finished
-    uint32_t pad[60];
+    uint32_t amax2_bits;  // second output's amax (dual quantizer: max |RHT(x)|)
+    uint32_t pad[59];
 };
 static_assert(sizeof(Workspace) == 256, "workspace layout");
 
@@ -27,6 +28,7 @@ struct QuantParams {
     int64_t rows, cols;     // logical matrix of the input (rows x cols, or T x C)
     int64_t ntiles;         // tiles in the whole tensor
     int64_t tiles_c;        // tiles along the contiguous axis
+    int64_t tiles_r;        // tiles along the strided axis (ntiles / tiles_c)
     uint8_t* q;             // codes
     uint8_t* sf;            // scales
     uint8_t* qT;            // transposed codes (2-D variant) or nullptr
@@ -35,9 +37,15 @@ struct QuantParams {
     uint64_t sr_seed;
     uint32_t rht_signs;     // 16 sign bits (Hadamard variant)
     int mode;               // nvfp4_round
+    // second output of the dual quantizer (Hadamard, token-major codes)
+    uint8_t* q2;
+    uint8_t* sf2;
+    float* g_dec2;
+    uint64_t sr_seed2;
+    int mode2;
 };
 
-enum class QuantKind { k1x16, k2d, kRht };
+enum class QuantKind { k1x16, k2d, kRht, kDual };
 
 // Host launchers (quantize.cu, gemm.cu, probe.cu).  They assume the
 // arguments were validated by the C-ABI layer.

@@ -23,6 +23,8 @@
 //   OpRht  — 64 tokens x 128 channels, 16-point random Hadamard transform
 //            along tokens, quantized along tokens and written channel-major
 //            ("Metodología de Entrenamiento": random Hadamard transforms).
+//   OpDual — the 1x16 and the Hadamard outputs of one tensor from one read,
+//            each with its own tensor scale (two amaxes reduced in phase 1).
 //
 // Floating-point order is fixed and identical to the oracle: IEEE division
 // and multiplication with round-to-nearest (__fdiv_rn/__fmul_rn), no FMA
@@ -41,9 +43,9 @@ constexpr int kMaxStages = 14;
 struct SmemCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    uint32_t warp_amax[kConsumerWarps];
-    float ftab[128];  // ftab[b] = rn(s_enc / E4M3value(b)) for every non-zero scale byte b
-    float amax;
+    uint32_t warp_amax[2][kConsumerWarps];
+    float ftab[2][128];  // ftab[o][b] = rn(s_enc[o] / E4M3value(b)) for every non-zero scale byte b
+    float amax[2];
     int abort;
 };
 
@@ -52,6 +54,16 @@ constexpr size_t kSmemBytes = 1024 + (size_t)kMaxStages * kTileBytes + sizeof(Sm
 // Swizzled (128-byte) address of 16-byte chunk `c` of row `r` in a tile whose
 // rows are 128 bytes.
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+
+// Tile index -> (index along the strided axis, index along the contiguous
+// axis) in 32-bit arithmetic (tile counts stay far below 2^32).
+__device__ __forceinline__ void tile_coords(int64_t t, const QuantParams& p, int64_t& major, int64_t& minor)
+{
+    const uint32_t tt = (uint32_t)t, tc = (uint32_t)p.tiles_c;
+    const uint32_t q = tt / tc;
+    major = q;
+    minor = tt - q * tc;
+}
 
 // --------------------------------------------------------- block quantize ----
 // Scale and round one block of 16 binary32 values.  Returns the scale byte;
@@ -140,19 +152,21 @@ struct Op1x16 {
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
                                  const QuantParams& p)
     {
-        const int64_t tr = tile / p.tiles_c, tc = tile % p.tiles_c;
+        int64_t tr, tc;
+        tile_coords(tile, p, tr, tc);
         tma_load_2d(dst, m, bar, (int32_t)(tc * 64), (int32_t)(tr * 128));
     }
 
-    __device__ static uint32_t phase1(const uint8_t* tile, int ctid, const QuantParams&)
+    __device__ static uint2 phase1(const uint8_t* tile, int ctid, const QuantParams&)
     {
-        return __float_as_uint(hmax_to_float(scan_tile_bf16(tile, ctid)));
+        return make_uint2(__float_as_uint(hmax_to_float(scan_tile_bf16(tile, ctid))), 0u);
     }
 
-    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const float* ftab,
-                                  const QuantParams& p)
+    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, const float (&s_enc)[2],
+                                  const float (*ftab)[128], const QuantParams& p)
     {
-        const int64_t tr = t / p.tiles_c, tc = t % p.tiles_c;
+        int64_t tr, tc;
+        tile_coords(t, p, tr, tc);
         const int lane = ctid & 31;
         const uint32_t row = (uint32_t)ctid >> 2, blk = ctid & 3;
         const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
@@ -169,7 +183,7 @@ struct Op1x16 {
         const int64_t grow = tr * 128 + row;
         const int64_t gcol = tc * 64 + blk * 16;
         uint32_t lo32, hi32;
-        const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc, ftab, p.mode, p.sr_seed,
+        const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc[0], ftab[0], p.mode, p.sr_seed,
                                           (uint64_t)(grow * (p.cols / 16) + gcol / 16), lo32, hi32);
         if (grow < p.rows && gcol < p.cols)
             *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
@@ -214,15 +228,16 @@ struct Op2d {
         Op1x16::issue(m, dst, bar, tile, p);
     }
 
-    __device__ static uint32_t phase1(const uint8_t* tile, int ctid, const QuantParams& p)
+    __device__ static uint2 phase1(const uint8_t* tile, int ctid, const QuantParams& p)
     {
         return Op1x16::phase1(tile, ctid, p);
     }
 
-    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const float* ftab,
-                                  const QuantParams& p)
+    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, const float (&s_enc)[2],
+                                  const float (*ftab)[128], const QuantParams& p)
     {
-        const int64_t tr = t / p.tiles_c, tc = t % p.tiles_c;
+        int64_t tr, tc;
+        tile_coords(t, p, tr, tc);
         const int lane = ctid & 31, cw = ctid >> 5;
         const int64_t kblocksT = p.rows / 16;
         const int64_t cpT = (kblocksT + 3) / 4;
@@ -247,7 +262,7 @@ struct Op2d {
         const int64_t grow = tr * 128 + row;
         const int64_t gcol = tc * 64 + blk * 16;
         uint32_t lo32, hi32;
-        const uint32_t sb = quant_block16(x, __uint_as_float(m), s_enc, ftab, NVFP4_ROUND_RN, 0, 0, lo32, hi32);
+        const uint32_t sb = quant_block16(x, __uint_as_float(m), s_enc[0], ftab[0], NVFP4_ROUND_RN, 0, 0, lo32, hi32);
         if (grow < p.rows && gcol < p.cols)
             *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
         p.sf[(tr * p.tiles_c + tc) * 512 + (row & 31) * 16 + (row >> 5) * 4 + blk] = (uint8_t)sb;
@@ -281,7 +296,8 @@ struct OpRht {
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
                                  const QuantParams& p)
     {
-        const int64_t tt = tile / p.tiles_c, ct = tile % p.tiles_c;
+        int64_t tt, ct;
+        tile_coords(tile, p, tt, ct);
         tma_load_2d(dst, m, bar, (int32_t)(ct * 128), (int32_t)(tt * 64));
         tma_load_2d(dst + 8192, m, bar, (int32_t)(ct * 128 + 64), (int32_t)(tt * 64));
     }
@@ -297,7 +313,7 @@ struct OpRht {
         for (int i = 0; i < 16; ++i) {
             const uint32_t row = tb * 16 + i;
             const uint32_t h = *reinterpret_cast<const uint16_t*>(half + sw128(row, cb >> 3) + (cb & 7) * 2);
-            y[i] = __uint_as_float((h << 16) ^ (((signs >> i) & 1u) << 31));
+            y[i] = __uint_as_float((h << 16) ^ ((signs << (31 - i)) & 0x80000000u));
         }
 #pragma unroll
         for (int hs = 1; hs < 16; hs <<= 1) {
@@ -315,7 +331,7 @@ struct OpRht {
             y[i] = __fmul_rn(y[i], 0.25f);
     }
 
-    __device__ static uint32_t phase1(const uint8_t* tile, int ctid, const QuantParams& p)
+    __device__ static uint32_t transformed_amax(const uint8_t* tile, int ctid, const QuantParams& p)
     {
         float y[16];
         transform(tile, ctid, p.rht_signs, y);
@@ -326,10 +342,18 @@ struct OpRht {
         return m;
     }
 
-    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, float s_enc, const float* ftab,
-                                  const QuantParams& p)
+    __device__ static uint2 phase1(const uint8_t* tile, int ctid, const QuantParams& p)
     {
-        const int64_t tt = t / p.tiles_c, ct = t % p.tiles_c;
+        return make_uint2(transformed_amax(tile, ctid, p), 0u);
+    }
+
+    // Quantize this thread's transformed channel block into (q, sf) with the
+    // given tensor scale.
+    __device__ static void quantize_out(const uint8_t* tile, int64_t t, int ctid, float s_enc, const float* ftab,
+                                        int mode, uint64_t seed, uint8_t* q, uint8_t* sf, const QuantParams& p)
+    {
+        int64_t tt, ct;
+        tile_coords(t, p, tt, ct);
         const int lane = ctid & 31, cw = ctid >> 5;
         const uint32_t tb = cw >> 2, cl = (cw & 3) * 32 + lane;
         const int64_t T = p.rows, C = p.cols;
@@ -345,10 +369,107 @@ struct OpRht {
         const int64_t kb = tt * 4 + tb;
         uint32_t lo32, hi32;
         const uint32_t sb =
-            quant_block16(y, bamax, s_enc, ftab, p.mode, p.sr_seed, (uint64_t)(c * kblocks + kb), lo32, hi32);
+            quant_block16(y, bamax, s_enc, ftab, mode, seed, (uint64_t)(c * kblocks + kb), lo32, hi32);
         if (c < C && kb < kblocks)
-            *reinterpret_cast<uint2*>(p.q + c * (T / 2) + kb * 8) = make_uint2(lo32, hi32);
-        p.sf[(ct * cp + tt) * 512 + (cl & 31) * 16 + (cl >> 5) * 4 + tb] = (uint8_t)sb;
+            *reinterpret_cast<uint2*>(q + c * (T / 2) + kb * 8) = make_uint2(lo32, hi32);
+        sf[(ct * cp + tt) * 512 + (cl & 31) * 16 + (cl >> 5) * 4 + tb] = (uint8_t)sb;
+    }
+
+    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, const float (&s_enc)[2],
+                                  const float (*ftab)[128], const QuantParams& p)
+    {
+        quantize_out(tile, t, ctid, s_enc[0], ftab[0], p.mode, p.sr_seed, p.q, p.sf, p);
+    }
+};
+
+// ------------------------------------------------------------------ dual ----
+// Both quantizations of an activation or gradient from one read: 1x16 blocks
+// along channels written row-major (q, sf; the Fprop/Dgrad operand) and the
+// Hadamard-transformed 16-token blocks written channel-major (q2, sf2; the
+// Wgrad operand), each with its own tensor scale.  Tile = 64 tokens x 128
+// channels (the Hadamard op's tile); consumer thread ctid owns the 1x16 block
+// (token (ctid % 256) / 4, channels 64 (ctid / 256) + 16 (ctid % 4) ..) and
+// the Hadamard column of OpRht.
+struct OpDual {
+    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
+                                 const QuantParams& p)
+    {
+        OpRht::issue(m, dst, bar, tile, p);
+    }
+
+    __device__ static const uint8_t* row_block(const uint8_t* tile, int ctid, uint32_t& row, uint32_t& box,
+                                               uint32_t& blk)
+    {
+        box = (uint32_t)ctid >> 8;
+        row = ((uint32_t)ctid & 255u) >> 2;
+        blk = (uint32_t)ctid & 3u;
+        return tile + box * 8192;
+    }
+
+    __device__ static uint2 phase1(const uint8_t* tile, int ctid, const QuantParams& p)
+    {
+        uint32_t row, box, blk;
+        const uint8_t* half = row_block(tile, ctid, row, box, blk);
+        const uint4 a = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk));
+        const uint4 b = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk + 1));
+        uint32_t acc = habs_max2(0u, a.x);
+        acc = habs_max2(acc, a.y);
+        acc = habs_max2(acc, a.z);
+        acc = habs_max2(acc, a.w);
+        acc = habs_max2(acc, b.x);
+        acc = habs_max2(acc, b.y);
+        acc = habs_max2(acc, b.z);
+        acc = habs_max2(acc, b.w);
+        return make_uint2(__float_as_uint(hmax_to_float(acc)), OpRht::transformed_amax(tile, ctid, p));
+    }
+
+    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, const float (&s_enc)[2],
+                                  const float (*ftab)[128], const QuantParams& p)
+    {
+        int64_t tt, ct;
+        tile_coords(t, p, tt, ct);
+        const int64_t T = p.rows, C = p.cols;
+        const int lane = ctid & 31;
+        uint32_t row, box, blk;
+        const uint8_t* half = row_block(tile, ctid, row, box, blk);
+        const uint4 a = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk));
+        const uint4 b = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk + 1));
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float x[16];
+        uint32_t acc = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            x[2 * j] = bf16lo(w[j]);
+            x[2 * j + 1] = bf16hi(w[j]);
+            acc = habs_max2(acc, w[j]);
+        }
+        const int64_t tok = tt * 64 + row;
+        const int64_t c0 = ct * 128 + box * 64 + blk * 16;
+        uint32_t lo32, hi32;
+        const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc[0], ftab[0], p.mode, p.sr_seed,
+                                          (uint64_t)(tok * (C / 16) + c0 / 16), lo32, hi32);
+        if (tok < T && c0 < C)
+            *reinterpret_cast<uint2*>(p.q + tok * (C / 2) + c0 / 2) = make_uint2(lo32, hi32);
+        // the 4 blocks of this token in this 64-channel group sit in lanes 4i..4i+3
+        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
+        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
+        const int64_t cp = (C / 16 + 3) / 4;  // 4-block groups per token row
+        const int64_t kg = ct * 2 + box;      // this 64-channel group
+        if ((lane & 3) == 0 && kg < cp) {
+            const int64_t tr = tok >> 7;      // 128-token row tile of the atom
+            const uint32_t r128 = (uint32_t)(tok & 127);
+            const int64_t atom = (tr * cp + kg) * 512;
+            *reinterpret_cast<uint32_t*>(p.sf + atom + (r128 & 31) * 16 + (r128 >> 5) * 4) =
+                sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            // with an odd count of 64-token tiles, rows 64..127 of the last
+            // atom are padding: write their zeros
+            if ((p.tiles_r & 1) && tt == p.tiles_r - 1) {
+                const uint32_t rp = r128 + 64;
+                *reinterpret_cast<uint32_t*>(p.sf + atom + (rp & 31) * 16 + (rp >> 5) * 4) = 0u;
+            }
+        }
+        OpRht::quantize_out(tile, t, ctid, s_enc[1], ftab[1], p.mode2, p.sr_seed2, p.q2, p.sf2, p);
     }
 };
 
@@ -402,12 +523,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------------------------------------- consumers ----
     const int ctid = threadIdx.x;  // 0 .. kConsumers-1
-    uint32_t amax_bits = 0;
+    uint2 amax_bits = make_uint2(0u, 0u);
     for (int64_t i = 0; i < n; ++i) {
         const int s = (int)(i % stages);
         if (!mbar_wait(&ctl->full[s], (uint32_t)((i / stages) & 1), ws, &ctl->abort))
             break;
-        amax_bits = max(amax_bits, Op::phase1(smem + (size_t)s * kTileBytes, ctid, p));
+        const uint2 m = Op::phase1(smem + (size_t)s * kTileBytes, ctid, p);
+        amax_bits.x = max(amax_bits.x, m.x);
+        amax_bits.y = max(amax_bits.y, m.y);
         if (i < n - R) {
             __syncwarp();
             if (lane == 0)
@@ -415,16 +538,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, off));
-    if (lane == 0)
-        ctl->warp_amax[warp] = amax_bits;
+    for (int off = 16; off > 0; off >>= 1) {
+        amax_bits.x = max(amax_bits.x, __shfl_xor_sync(0xFFFFFFFFu, amax_bits.x, off));
+        amax_bits.y = max(amax_bits.y, __shfl_xor_sync(0xFFFFFFFFu, amax_bits.y, off));
+    }
+    if (lane == 0) {
+        ctl->warp_amax[0][warp] = amax_bits.x;
+        ctl->warp_amax[1][warp] = amax_bits.y;
+    }
     named_bar_sync(1, kConsumers);
     if (ctid == 0) {
-        uint32_t m = 0;
-        for (int w = 0; w < kConsumerWarps; ++w)
-            m = max(m, ctl->warp_amax[w]);
-        atomicMax(&ws->amax_bits, m);
+        uint32_t m0 = 0, m1 = 0;
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            m0 = max(m0, ctl->warp_amax[0][w]);
+            m1 = max(m1, ctl->warp_amax[1][w]);
+        }
+        atomicMax(&ws->amax_bits, m0);
+        atomicMax(&ws->amax2_bits, m1);
         __threadfence();
         atomicAdd(&ws->arrived, 1u);
         const uint64_t t0 = global_ns();
@@ -435,19 +565,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __nanosleep(64);
         }
-        const uint32_t am = ld_acquire_gpu(&ws->amax_bits);
-        if (am >= 0x7F800000u)
+        const uint32_t am0 = ld_acquire_gpu(&ws->amax_bits);
+        const uint32_t am1 = ld_acquire_gpu(&ws->amax2_bits);
+        if (am0 >= 0x7F800000u || am1 >= 0x7F800000u)
             record_status(ws, NVFP4_ERR_NONFINITE);
-        ctl->amax = __uint_as_float(am);
+        ctl->amax[0] = __uint_as_float(am0);
+        ctl->amax[1] = __uint_as_float(am1);
     }
     named_bar_sync(1, kConsumers);
 
-    float s_enc, g;
-    tensor_scales(ctl->amax, s_enc, g);
-    if (bid == 0 && ctid == 0)
-        *p.g_dec = g;
-    if (ctid < 128)
-        ctl->ftab[ctid] = (ctid == 0 || ctid == 127) ? 0.0f : __fdiv_rn(s_enc, e4m3_value((uint32_t)ctid));
+    float s_enc[2], g[2];
+    tensor_scales(ctl->amax[0], s_enc[0], g[0]);
+    tensor_scales(ctl->amax[1], s_enc[1], g[1]);
+    if (bid == 0 && ctid == 0) {
+        *p.g_dec = g[0];
+        if (p.g_dec2)
+            *p.g_dec2 = g[1];
+    }
+    if (ctid < 256) {
+        const int o = ctid >> 7, b = ctid & 127;
+        ctl->ftab[o][b] = (b == 0 || b == 127) ? 0.0f : __fdiv_rn(s_enc[o], e4m3_value((uint32_t)b));
+    }
     named_bar_sync(1, kConsumers);
 
     volatile int* abort_flag = &ctl->abort;
@@ -469,6 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t old = atomicAdd(&ws->departed, 1u);
         if (old == (uint32_t)G - 1) {
             ws->amax_bits = 0;
+            ws->amax2_bits = 0;
             ws->arrived = 0;
             ws->departed = 0;
             __threadfence();
@@ -518,10 +657,10 @@ nvfp4_status launch_quantize(QuantKind kind, const void* x, int64_t ld, const Qu
                              cudaStream_t stream)
 {
     CUtensorMap map;
+    const bool token_tiles = kind == QuantKind::kRht || kind == QuantKind::kDual;  // 64 x 64 boxes
     const bool ok = encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(x),
-                                         (uint64_t)p.cols, (uint64_t)p.rows, (uint64_t)ld * 2u,
-                                         kind == QuantKind::kRht ? 64u : 64u, kind == QuantKind::kRht ? 64u : 128u,
-                                         CU_TENSOR_MAP_SWIZZLE_128B);
+                                         (uint64_t)p.cols, (uint64_t)p.rows, (uint64_t)ld * 2u, 64u,
+                                         token_tiles ? 64u : 128u, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok)
         return NVFP4_ERR_CUDA;
     switch (kind) {
@@ -531,6 +670,8 @@ nvfp4_status launch_quantize(QuantKind kind, const void* x, int64_t ld, const Qu
         return launch_fused<Op2d>(map, p, ws, stream);
     case QuantKind::kRht:
         return launch_fused<OpRht>(map, p, ws, stream);
+    case QuantKind::kDual:
+        return launch_fused<OpDual>(map, p, ws, stream);
     }
     return NVFP4_ERR_ARG;
 }

@@ -4,6 +4,7 @@
   python -m nvfp4_bit_quantized_quantize_gb300.profile_case quantize ROWS COLS rn|sr [reps]
   python -m nvfp4_bit_quantized_quantize_gb300.profile_case quantize_2d ROWS COLS [reps]
   python -m nvfp4_bit_quantized_quantize_gb300.profile_case rht T C rn|sr [reps]
+  python -m nvfp4_bit_quantized_quantize_gb300.profile_case dual T C rn|sr [reps]
 
 Inputs are made on the device (random codes and E4M3 scales for the GEMM,
 N(0,1) bf16 for the quantizers); each case runs 2 warm-up launches and then
@@ -52,7 +53,7 @@ def main(argv):
     else:
         R, C = int(argv[1]), int(argv[2])
         mode = nv.SR if (len(argv) > 3 and argv[3] == "sr") else nv.RN
-        rest = argv[4:] if kind in ("quantize", "rht") else argv[3:]
+        rest = argv[4:] if kind in ("quantize", "rht", "dual") else argv[3:]
         reps = int(rest[0]) if rest else 3
         x = torch.randn((R, C), dtype=torch.bfloat16, device="cuda")
         if kind == "quantize":
@@ -65,6 +66,10 @@ def main(argv):
         elif kind == "rht":
             q, sf, g = nv.alloc_quantized(C, R)
             fn = lambda: nv.nvfp4_rht_quantize(x, R, C, C, 5, mode, 1, q, sf, g, ws)
+        elif kind == "dual":
+            q, sf, g = nv.alloc_quantized(R, C)
+            qT, sfT, gT = nv.alloc_quantized(C, R)
+            fn = lambda: nv.nvfp4_quantize_dual(x, R, C, C, mode, 1, q, sf, g, 5, mode, 2, qT, sfT, gT, ws)
         else:
             raise SystemExit(__doc__)
         ms = _time(fn, reps)

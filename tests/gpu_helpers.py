@@ -61,6 +61,21 @@ def rht_quantize(x_bits, rht_seed, mode=nv.SR, sr_seed=0, ld=None, ws=None):
     return qT.cpu().numpy(), sfT.cpu().numpy(), float(g.cpu()[0]), st
 
 
+def quantize_dual(x_bits, mode, sr_seed, rht_seed, mode_t, sr_seed_t, ld=None, ws=None):
+    T, C = x_bits.shape
+    x = dev_bf16(x_bits, ld)
+    q, sf, g = nv.alloc_quantized(T, C)
+    qT, sfT, gT = nv.alloc_quantized(C, T)
+    for t in (q, sf, qT, sfT):
+        t.fill_(0xEE)
+    ws = nv.alloc_workspace() if ws is None else ws
+    nv.nvfp4_quantize_dual(x, T, C, x.shape[1], mode, sr_seed, q, sf, g, rht_seed, mode_t, sr_seed_t,
+                           qT, sfT, gT, ws)
+    st = nv.nvfp4_device_status(ws)
+    return (q.cpu().numpy(), sf.cpu().numpy(), float(g.cpu()[0]),
+            qT.cpu().numpy(), sfT.cpu().numpy(), float(gT.cpu()[0]), st)
+
+
 def gemm(qa, sfa, ga, qb, sfb, gb, M, N, K, out_f32=False, ws=None):
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     d = torch.empty((M, N), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")

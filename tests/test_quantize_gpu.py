@@ -10,7 +10,7 @@ import oracle as O
 import nvfp4_bit_quantized_quantize_gb300 as nv
 from nvfp4_bit_quantized_quantize_gb300 import synth
 
-from gpu_helpers import quantize, quantize_2d, rht_quantize
+from gpu_helpers import quantize, quantize_2d, quantize_dual, rht_quantize
 
 pytestmark = pytest.mark.gpu
 
@@ -127,6 +127,34 @@ def test_rht_quantize_parity(shape, mode):
     _assert_same(sfT, rsfT, "scales")
 
 
+@pytest.mark.parametrize("modes", [(nv.RN, nv.SR), (nv.SR, nv.RN)])
+@pytest.mark.parametrize("shape", [(64, 128), (48, 80), (272, 208), (16, 16), (1024, 384), (192, 1040)])
+def test_quantize_dual_parity(shape, modes):
+    """One read, two outputs: each equals the single-form oracle quantizer."""
+    mode, mode_t = modes
+    x = synth.normal_bf16(shape, 41, shape[1] % 5, 1.0, 0.0, 0.01, 30.0)
+    q, sf, g, qT, sfT, gT, st = quantize_dual(x, mode, 9, 123, mode_t, 10)
+    rq, rsf, rg = O.quantize(x, mode, 9)
+    rqT, rsfT, rgT = O.rht_quantize(x, 123, mode_t, 10)
+    assert st == 0 and g == rg and gT == rgT
+    _assert_same(q, rq, "row codes")
+    _assert_same(sf, rsf, "row scales")
+    _assert_same(qT, rqT, "transformed codes")
+    _assert_same(sfT, rsfT, "transformed scales")
+
+
+def test_quantize_dual_leading_dimension():
+    x = synth.normal_bf16((128, 96), 42, 0, 1.0)
+    q, sf, g, qT, sfT, gT, st = quantize_dual(x, nv.RN, 0, 3, nv.SR, 4, ld=136)
+    rq, rsf, rg = O.quantize(x, O.RN, 0)
+    rqT, rsfT, rgT = O.rht_quantize(x, 3, O.SR, 4)
+    assert st == 0 and g == rg and gT == rgT
+    _assert_same(q, rq, "row codes")
+    _assert_same(sf, rsf, "row scales")
+    _assert_same(qT, rqT, "transformed codes")
+    _assert_same(sfT, rsfT, "transformed scales")
+
+
 # ---------------------------------------------- full-size workload tensors ----
 
 @pytest.mark.parametrize("name", ["A1024", "A4096", "A8192"])
@@ -160,3 +188,18 @@ def test_rht_sr_full_size_wgrad_workload():
     assert st == 0 and g == rg
     _assert_same(qT, rqT, "codes")
     _assert_same(sfT, rsfT, "scales")
+
+
+def test_quantize_dual_full_size_activation():
+    """The MLP input X [8192, 4096] (outlier channels): forward RN row form
+    and the Hadamard SR form, as the MLP step quantizes it."""
+    wl = synth.make_workload("mlp7b_fwd_bwd_h4096_f11008_t8192", only={"X"})
+    x = wl["X"]
+    q, sf, g, qT, sfT, gT, st = quantize_dual(x, nv.RN, 0, 17, nv.SR, 18)
+    rq, rsf, rg = O.quantize(x, O.RN, 0)
+    rqT, rsfT, rgT = O.rht_quantize(x, 17, O.SR, 18)
+    assert st == 0 and g == rg and gT == rgT
+    _assert_same(q, rq, "row codes")
+    _assert_same(sf, rsf, "row scales")
+    _assert_same(qT, rqT, "transformed codes")
+    _assert_same(sfT, rsfT, "transformed scales")
