@@ -409,9 +409,74 @@ def run_ours(args, rank, world, local_rank):
                        "note": "pinned host inputs copied in and results copied out every step; copies on "
                                "separate streams overlap the neighbouring steps' compute (two device slots)"}
 
+    if not args.no_extras:
+        line["extras"] = measure_extras(step, stream, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     return line
+
+
+def _event_ms(fn, stream, reps=10, warmup=3):
+    """Mean CUDA-event time of fn() on `stream` after warm-up."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def measure_extras(step, stream, pk):
+    """Kernels beside the step, each timed alone (not part of `value`):
+    the quantization-noise meter on H's forward form, a GEMM with ragged
+    M, N, K, and cuBLAS bf16 matmul on the step's six GEMM shapes for context."""
+    import torch
+
+    nv = step.nv
+    T, D, F = TOKENS, HIDDEN, FFN
+    dev = step.dev
+    out = {}
+    # noise meter: reads H (bf16) + its codes + scales once: 2.5625 B/element
+    sums = torch.empty(2, dtype=torch.float64, device=dev)
+    q, sf, g = step.hq
+    ms = _event_ms(lambda: nv.nvfp4_quant_noise(step.H, T, F, F, q, sf, g, sums), stream)
+    byts = 2.5625 * T * F
+    out["quant_noise[8192x11008]"] = {"ms": round(ms, 4), "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
+                                      "frac": round(byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+                                      "norm_ratio": round(float((sums[1] / sums[0]).sqrt()), 3)}
+    # ragged GEMM: every dimension off the tile grid
+    M, N, K = 8000, 11000, 4064
+    a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev)
+    b = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev)
+    sfa = torch.randint(0x30, 0x48, (nv.nvfp4_sf_bytes(M, K),), dtype=torch.uint8, device=dev)
+    sfb = torch.randint(0x30, 0x48, (nv.nvfp4_sf_bytes(N, K),), dtype=torch.uint8, device=dev)
+    one = torch.ones(1, device=dev)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ms = _event_ms(lambda: nv.nvfp4_gemm(a, sfa, one, b, sfb, one, M, N, K, d, N, nv.OUT_BF16, step.ws), stream)
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    out[f"gemm_ragged[{M}x{N}x{K}]"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1)}
+    del a, b, sfa, sfb, d
+    # cuBLAS bf16 on the same six GEMMs (context: the unquantized layer)
+    shapes = [(T, F, D), (T, D, F), (T, F, D), (D, F, T), (T, D, F), (F, D, T)]
+    tot = 0.0
+    for (m, n, k) in shapes:
+        x = torch.randn((m, k), dtype=torch.bfloat16, device=dev)
+        w = torch.randn((n, k), dtype=torch.bfloat16, device=dev)
+        tot += _event_ms(lambda: torch.matmul(x, w.t()), stream, reps=5)
+        del x, w
+    out["cublas_bf16_six_gemms"] = {"ms": round(tot, 4),
+                                    "TFLOP/s": round(N_GEMMS * GEMM_FLOPS / (tot * 1e-3) / 1e12, 1)}
+    st = nv.nvfp4_device_status(step.ws)
+    if st != 0:
+        raise RuntimeError(f"device status after extras: {nv.nvfp4_status_str(st)}")
+    return out
 
 
 # ------------------------------------------------------- CPU oracle arm ----
@@ -504,6 +569,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -159,6 +159,27 @@ nvfp4_status nvfp4_quantize_dual(const void* x, int64_t T, int64_t C, int64_t ld
                                  void* ws, nvfp4_stream_t stream);
 
 /*
+ * Quantization-noise meter ["FP4 All the Way", "Describir": quantized
+ * training loses efficiency once the gradient norm falls below about
+ * sqrt(3) times the quantization noise].  For x [rows, cols] (bf16, leading
+ * dimension ld) and its 1x16 form (q, sf, g_dec) as nvfp4_quantize, the row
+ * outputs of nvfp4_quantize_2d or nvfp4_quantize_dual write it:
+ *   sums[0] = sum over all elements of (Q(x) - x)^2,
+ *             Q(x) = E2M1(code) * E4M3(scale) * g_dec,
+ *   sums[1] = sum of x^2,
+ * so ||x|| / ||Q(x) - x|| = sqrt(sums[1] / sums[0]) is compared with sqrt(3).
+ * sums: 2 doubles of DEVICE memory (8-byte aligned), overwritten (the call
+ * zeroes them on `stream` first).  Elements are differenced in binary32
+ * (one fused multiply-add each), blocks summed in binary32 and totals kept in
+ * binary64; the order of the totals is not fixed (relative differences of a
+ * few 1e-7 between runs).  cols % 16 == 0.  Non-finite x gives non-finite
+ * sums.  No workspace needed.
+ */
+nvfp4_status nvfp4_quant_noise(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                               const uint8_t* q, const uint8_t* sf, const float* g_dec,
+                               double* sums, nvfp4_stream_t stream);
+
+/*
  * Block-scaled NVFP4 matmul on the tcgen05 tensor cores [NVFP4 is supported
  * by Blackwell tensor cores: "Entrenamiento ...", "El Desafío de la
  * Precisión de 4 Bits"].
@@ -168,8 +189,14 @@ nvfp4_status nvfp4_quantize_dual(const void* x, int64_t T, int64_t C, int64_t ld
  *   a, sfa  [M, K/2] codes + nvfp4_sf_bytes(M, K) scales (K contiguous)
  *   b, sfb  [N, K/2] codes + nvfp4_sf_bytes(N, K) scales (K contiguous)
  *   ga, gb  device floats (the quantizers' g_dec)
- *   d       out: [M, N] row-major, leading dimension ldd (elements)
- * Shapes: M % 128 == 0, N % 128 == 0, K % 64 == 0 (all > 0).
+ *   d       out: [M, N] row-major, leading dimension ldd (elements); ldd
+ *           times the element size a multiple of 16 bytes
+ * Shapes: M, N, K > 0 and K % 32 == 0 (a code row must be a whole number of
+ * 16-byte units for the tensor copies).  Ragged M, N and K are handled: the
+ * last tiles are padded on chip and only rows < M, columns < N are written.
+ * The padding bytes of sfa and sfb (past row M / N, past K/16 in the last
+ * 4-block group) must not be NaN codes (0x7F, 0xFF); the quantizers write
+ * zeros there.
  */
 nvfp4_status nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga,
                         const uint8_t* b, const uint8_t* sfb, const float* gb,

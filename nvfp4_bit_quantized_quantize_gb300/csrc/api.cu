@@ -260,6 +260,22 @@ nvfp4_status nvfp4_quantize_dual(const void* x, int64_t T, int64_t C, int64_t ld
     return launch_quantize(QuantKind::kDual, x, ld, p, static_cast<Workspace*>(ws), (cudaStream_t)stream);
 }
 
+nvfp4_status nvfp4_quant_noise(const void* x, int64_t rows, int64_t cols, int64_t ld, const uint8_t* q,
+                               const uint8_t* sf, const float* g_dec, double* sums, nvfp4_stream_t stream)
+{
+    if (!x || !q || !sf || !g_dec || !sums)
+        return NVFP4_ERR_ARG;
+    if (rows <= 0 || cols <= 0 || cols % 16 != 0 || ld < cols || rows > (1ll << 31) || cols > (1ll << 31))
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sf) || ld % 8 != 0 || (reinterpret_cast<uintptr_t>(sums) & 7) ||
+        (reinterpret_cast<uintptr_t>(g_dec) & 3))
+        return NVFP4_ERR_ALIGN;
+    nvfp4_status st = check_device();
+    if (st != NVFP4_OK)
+        return st;
+    return launch_quant_noise(x, rows, cols, ld, q, sf, g_dec, sums, (cudaStream_t)stream);
+}
+
 nvfp4_status nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
                         const uint8_t* sfb, const float* gb, int64_t M, int64_t N, int64_t K, void* d, int64_t ldd,
                         nvfp4_out_dtype out_dtype, void* ws, nvfp4_stream_t stream)
@@ -267,7 +283,7 @@ nvfp4_status nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, c
     if (!a || !sfa || !ga || !b || !sfb || !gb || !d || !ws ||
         (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32))
         return NVFP4_ERR_ARG;
-    if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 128 != 0 || K % 64 != 0 || ldd < N ||
+    if (M <= 0 || N <= 0 || K <= 0 || K % 32 != 0 || ldd < N ||
         K / 2 >= (1ll << 32) || M > (1ll << 31) || N > (1ll << 31))
         return NVFP4_ERR_SHAPE;
     if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d) || !aligned16(ws) ||

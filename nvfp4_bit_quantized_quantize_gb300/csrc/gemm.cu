@@ -5,7 +5,10 @@
 //   D[m, n] = ga * gb * sum_k A(m, k) * B(n, k)
 //
 // A [M, K] and B [N, K] are packed E2M1 codes (K contiguous) with one E4M3
-// scale per 16 elements in the 128 x 4 atom layout.  Each CTA owns a
+// scale per 16 elements in the 128 x 4 atom layout.  Ragged M, N and K are
+// padded on chip: tensor loads past the edges read zeros, the scale buffers'
+// padding (zero, as the quantizers write it) covers the last atoms, and the
+// output tensor store drops rows and columns past M and N.  Each CTA owns a
 // persistent sequence of 128 x 256 output tiles:
 //   warp 0  TMA producer: A/B tiles (128-byte swizzle) and the scale atoms
 //           (bulk copies) into a 4-stage shared-memory ring;
@@ -74,6 +77,14 @@ struct GemmArgs {
     int32_t out_f32;
 };
 
+// A 32-row x `width`-column output chunk that crosses the M or N edge is
+// written with plain stores instead of a tensor store, so that nothing outside
+// M x N is touched whatever the tensor unit does with a partial 16-byte unit.
+__device__ __forceinline__ bool edge_chunk(int32_t col, int32_t width, int32_t row0, const GemmArgs& a)
+{
+    return col + width > a.N || row0 + 32 > a.M;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -91,11 +102,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &ctl->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t tiles_m = (uint32_t)args.M / BM;
+    const uint32_t tiles_m = ((uint32_t)args.M + BM - 1) / BM;
     const uint32_t tiles_n = ((uint32_t)args.N + BN - 1) / BN;
     const uint32_t ntiles = tiles_m * tiles_n;
     const uint32_t kstages = ((uint32_t)args.K + BK - 1) / BK;
     const uint32_t cp = ((uint32_t)args.K / 16 + 3) / 4;  // scale atoms along K
+    const uint32_t nrows_b = ((uint32_t)args.N + 127) / 128;  // 128-row scale tiles of B
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -124,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
             const uint32_t tm = t % tiles_m, tn = t / tiles_m;
             const int32_t m0 = (int32_t)(tm * BM), n0 = (int32_t)(tn * BN);
-            const uint32_t nrt = (args.N - n0) >= 256 ? 2u : 1u;  // 128-row scale tiles present in B
+            const uint32_t nrt = 2 * tn + 1 < nrows_b ? 2u : 1u;  // 128-row scale tiles present in B
             const uint8_t* sfa_t = args.sfa + (size_t)tm * cp * 512;
             const uint8_t* sfb_t = args.sfb + (size_t)(2 * tn) * cp * 512;
             for (uint32_t ks = 0; ks < kstages; ++ks) {
@@ -192,7 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_nvf4(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, kIdesc, sfa_t + 4 * j,
                                  sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
                 } else {
-                    const uint32_t kk = k_left / 64;
+                    // last stage: K = 64 steps, the final one possibly half
+                    // filled (codes past K read as zeros, their scales are the
+                    // zero padding of the last atom)
+                    const uint32_t kk = (k_left + 63) / 64;
                     for (uint32_t j = 0; j < kk; ++j) {
                         tmem_cp_32x128b_x4(sfa_t + 4 * j, sfa_desc + off + 32 * j);
                         tmem_cp_32x128b_x4(sfb_t + 8 * j, sfb_desc + off + 32 * j);
@@ -239,17 +254,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&ctl->tmem_empty);
             if (c0 >= args.N)
                 continue;
-            uint8_t* buf = store_buf + (warp - 2) * kStoreBufBytes;
             const int32_t row0 = (int32_t)(tm * BM + q * 32);
+            if (row0 >= args.M)
+                continue;
+            uint8_t* buf = store_buf + (warp - 2) * kStoreBufBytes;
             if (args.out_f32) {
                 // 16 chunks of 8 columns (32 bytes per row)
 #pragma unroll
                 for (int ch = 0; ch < 16; ++ch) {
+                    if (c0 + ch * 8 >= args.N)
+                        break;
                     const uint32_t* rr = &r[ch >> 2][(ch & 3) * 8];
                     uint32_t w[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         w[e] = __float_as_uint(__fmul_rn(__uint_as_float(rr[e]), alpha));
+                    if (edge_chunk(c0 + ch * 8, 8, row0, args)) {
+                        // ragged edge: plain stores of the elements inside M x N
+                        const int32_t row = row0 + lane, col = c0 + ch * 8;
+                        if (row < args.M) {
+                            float* dst = static_cast<float*>(args.d) + (int64_t)row * args.ldd + col;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (col + e < args.N)
+                                    dst[e] = __uint_as_float(w[e]);
+                        }
+                        continue;
+                    }
                     if (lane == 0)
                         bulk_wait_read0();
                     __syncwarp();
@@ -266,12 +297,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // 8 chunks of 16 columns (32 bytes per row)
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
+                    if (c0 + ch * 16 >= args.N)
+                        break;
                     const uint32_t* rr = &r[ch >> 1][(ch & 1) * 16];
                     uint32_t w[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         w[e] = pack_bf16x2(__fmul_rn(__uint_as_float(rr[2 * e]), alpha),
                                            __fmul_rn(__uint_as_float(rr[2 * e + 1]), alpha));
+                    if (edge_chunk(c0 + ch * 16, 16, row0, args)) {
+                        const int32_t row = row0 + lane, col = c0 + ch * 16;
+                        if (row < args.M) {
+                            uint16_t* dst = static_cast<uint16_t*>(args.d) + (int64_t)row * args.ldd + col;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                if (col + e < args.N)
+                                    dst[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+                        }
+                        continue;
+                    }
                     if (lane == 0)
                         bulk_wait_read0();
                     __syncwarp();
@@ -329,7 +373,7 @@ nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, 
         attr_set[dev] = true;
     }
     GemmArgs args{sfa, sfb, ga, gb, d, ldd, (int32_t)M, (int32_t)N, (int32_t)K, dt == NVFP4_OUT_F32 ? 1 : 0};
-    const int64_t ntiles = (M / BM) * ((N + BN - 1) / BN);
+    const int64_t ntiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int sms = device_sm_count();
     const int grid = (int)(ntiles < sms ? ntiles : sms);
     nvf4_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, md, args, ws);

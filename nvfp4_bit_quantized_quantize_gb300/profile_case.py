@@ -5,6 +5,7 @@
   python -m nvfp4_bit_quantized_quantize_gb300.profile_case quantize_2d ROWS COLS [reps]
   python -m nvfp4_bit_quantized_quantize_gb300.profile_case rht T C rn|sr [reps]
   python -m nvfp4_bit_quantized_quantize_gb300.profile_case dual T C rn|sr [reps]
+  python -m nvfp4_bit_quantized_quantize_gb300.profile_case noise ROWS COLS [reps]
 
 Inputs are made on the device (random codes and E4M3 scales for the GEMM,
 N(0,1) bf16 for the quantizers); each case runs 2 warm-up launches and then
@@ -66,6 +67,11 @@ def main(argv):
         elif kind == "rht":
             q, sf, g = nv.alloc_quantized(C, R)
             fn = lambda: nv.nvfp4_rht_quantize(x, R, C, C, 5, mode, 1, q, sf, g, ws)
+        elif kind == "noise":
+            q, sf, g = nv.alloc_quantized(R, C)
+            nv.nvfp4_quantize(x, R, C, C, nv.RN, 0, q, sf, g, ws)
+            sums = torch.empty(2, dtype=torch.float64, device="cuda")
+            fn = lambda: nv.nvfp4_quant_noise(x, R, C, C, q, sf, g, sums)
         elif kind == "dual":
             q, sf, g = nv.alloc_quantized(R, C)
             qT, sfT, gT = nv.alloc_quantized(C, R)

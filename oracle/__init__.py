@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.or_gemm_f64_sampled.argtypes = [p, p, ctypes.c_float, p, p, ctypes.c_float,
                                           i64, i64, i64, p, p, i64, p, p]
         L.or_gemm_f64_sampled.restype = None
+        L.or_quant_noise.argtypes = [p, i64, i64, i64, p, p, ctypes.c_float, p]
+        L.or_quant_noise.restype = None
         L.or_e2m1_rn_many.argtypes = [p, i64, p]
         L.or_e2m1_sr_many.argtypes = [p, p, i64, p]
         L.or_e4m3_rn_sat_many.argtypes = [p, i64, p]
@@ -256,3 +258,13 @@ def gemm_f64_sampled(a, sfa, ga, b, sfb, gb, M, N, K, ms, ns):
     lib().or_gemm_f64_sampled(_ptr(a), _ptr(sfa), ga, _ptr(b), _ptr(sfb), gb, M, N, K,
                               _ptr(ms), _ptr(ns), ms.size, _ptr(d), _ptr(dabs))
     return d, dabs
+
+
+def quant_noise(x_bf16: np.ndarray, q: np.ndarray, sf: np.ndarray, g: float):
+    """(sum (Q(x) - x)^2, sum x^2) in binary64 for the 1x16 form (q, sf, g) of x."""
+    x = _c(x_bf16, np.uint16)
+    R, C = x.shape
+    q, sf = _c(q, np.uint8), _c(sf, np.uint8)
+    out = np.zeros(2, np.float64)
+    lib().or_quant_noise(_ptr(x), R, C, C, _ptr(q), _ptr(sf), g, _ptr(out))
+    return float(out[0]), float(out[1])

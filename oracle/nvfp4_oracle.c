@@ -537,6 +537,30 @@ void or_gemm_f64_sampled(const uint8_t* a, const uint8_t* sfa, float ga, const u
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* Quantization-noise meter [P2 "Describir": quantized training loses        */
+/* efficiency once the gradient norm falls below about sqrt(3) times the     */
+/* quantization noise].  Reading: the noise is the Euclidean norm of          */
+/* Q(x) - x over the tensor, Q(x) the decoded NVFP4 value; the gradient norm  */
+/* is the Euclidean norm of x.  sums[0] = sum (Q(x) - x)^2, sums[1] = sum x^2,*/
+/* both in binary64 (Q(x) = code * scale * g is exact in binary64).          */
+/* ------------------------------------------------------------------------ */
+
+void or_quant_noise(const uint16_t* x, int64_t R, int64_t C, int64_t ld, const uint8_t* q,
+                    const uint8_t* sf, float g, double sums[2])
+{
+    double se = 0.0, sx = 0.0;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            double xv = (double)bf16_to_f32(x[r * ld + c]);
+            double d = deq(q, sf, r, c, C) * (double)g - xv;
+            se += d * d;
+            sx += xv * xv;
+        }
+    sums[0] = se;
+    sums[1] = sx;
+}
+
 /* Batch helpers so tests can sweep the element codecs without a Python loop. */
 void or_e2m1_rn_many(const float* v, int64_t n, uint8_t* out)
 {

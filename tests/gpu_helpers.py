@@ -76,13 +76,37 @@ def quantize_dual(x_bits, mode, sr_seed, rht_seed, mode_t, sr_seed_t, ld=None, w
             qT.cpu().numpy(), sfT.cpu().numpy(), float(gT.cpu()[0]), st)
 
 
-def gemm(qa, sfa, ga, qb, sfb, gb, M, N, K, out_f32=False, ws=None):
+def gemm(qa, sfa, ga, qb, sfb, gb, M, N, K, out_f32=False, ws=None, ldd=None):
+    """Run the GEMM; the output rows are padded to ldd (a multiple of 16 bytes),
+    32 spare rows follow row M, all pre-filled with NaN, and the padding must
+    come back untouched."""
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    d = torch.empty((M, N), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    unit = 4 if out_f32 else 8
+    ldd = ((N + unit - 1) // unit) * unit if ldd is None else ldd
+    # 32 spare rows below M: a write past row M would land there
+    d = torch.full((M + 32, ldd), float("nan"), dtype=torch.float32 if out_f32 else torch.bfloat16,
+                   device="cuda")
     gat = torch.tensor([ga], dtype=torch.float32, device="cuda")
     gbt = torch.tensor([gb], dtype=torch.float32, device="cuda")
     ws = nv.alloc_workspace() if ws is None else ws
-    nv.nvfp4_gemm(t(qa), t(sfa), gat, t(qb), t(sfb), gbt, M, N, K, d, N,
+    nv.nvfp4_gemm(t(qa), t(sfa), gat, t(qb), t(sfb), gbt, M, N, K, d, ldd,
                   nv.OUT_F32 if out_f32 else nv.OUT_BF16, ws)
     st = nv.nvfp4_device_status(ws)
-    return d.float().cpu().numpy().astype(np.float64), st
+    out = d.float().cpu().numpy().astype(np.float64)
+    assert np.isnan(out[:M, N:]).all(), "GEMM wrote past column N"
+    assert np.isnan(out[M:]).all(), "GEMM wrote past row M"
+    return np.ascontiguousarray(out[:M, :N]), st
+
+
+def quant_noise(x_bits, q, sf, g, ld=None):
+    """The CUDA noise meter on host arrays: returns (sum (Q-x)^2, sum x^2)."""
+    rows, cols = x_bits.shape
+    x = dev_bf16(x_bits, ld)
+    qt = torch.from_numpy(np.ascontiguousarray(q)).cuda()
+    sft = torch.from_numpy(np.ascontiguousarray(sf)).cuda()
+    gt = torch.tensor([g], dtype=torch.float32, device="cuda")
+    sums = torch.full((2,), float("nan"), dtype=torch.float64, device="cuda")
+    nv.nvfp4_quant_noise(x, rows, cols, x.shape[1], qt, sft, gt, sums)
+    torch.cuda.synchronize()
+    s = sums.cpu().numpy()
+    return float(s[0]), float(s[1])

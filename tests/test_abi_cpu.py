@@ -70,8 +70,22 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.nvfp4_quantize_2d(fake, 24, 32, 32, fake, fake, fake, None, fake, fake, None) == 1
     assert L.nvfp4_quantize_2d(fake, 24, 32, 32, fake, fake, None, None, fake, fake, None) == 2
     assert L.nvfp4_rht_quantize(fake, 24, 32, 32, 1, 0, 0, fake, fake, fake, fake, None) == 2
-    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 100, 128, 64, fake, 128, 0, fake, None) == 2
-    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 128, 128, 96, fake, 128, 0, fake, None) == 2
+    # GEMM: any M, N > 0; K a positive multiple of 32
+    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 0, 128, 64, fake, 128, 0, fake, None) == 2
+    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 128, 0, 64, fake, 128, 0, fake, None) == 2
+    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 128, 128, 80, fake, 128, 0, fake, None) == 2
+    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 128, 128, 0, fake, 128, 0, fake, None) == 2
+    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 100, 130, 64, fake, 128, 0, fake, None) == 2
+    assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 100, 130, 64, fake, 134, 1, fake, None) == 3
     assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 128, 128, 64, fake, 128, 5, fake, None) == 1
     assert L.nvfp4_gemm(fake, fake, fake, fake, fake, fake, 128, 128, 64, fake, 132, 0, fake, None) == 3
+    # dual quantizer: T % 16 and C % 16
+    assert L.nvfp4_quantize_dual(fake, 32, 40, 40, 0, 0, fake, fake, fake, 1, 1, 0, fake, fake, fake, fake,
+                                 None) == 2
+    assert L.nvfp4_quantize_dual(fake, 24, 32, 32, 0, 0, fake, fake, fake, 1, 1, 0, fake, fake, fake, fake,
+                                 None) == 2
+    assert L.nvfp4_quantize_dual(fake, 32, 32, 32, 0, 0, fake, fake, fake, 1, 3, 0, fake, fake, fake, fake,
+                                 None) == 1
+    assert L.nvfp4_quantize_dual(fake, 32, 32, 32, 0, 0, fake, fake, fake, 1, 1, 0, None, fake, fake, fake,
+                                 None) == 1
     assert L.nvfp4_workspace_init(None, None) == 1

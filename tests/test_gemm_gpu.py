@@ -88,6 +88,37 @@ def test_gemm_shapes_full_compare(M, N, K):
         _check(d, ref, dabs, not f32, f"{M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 1, 32), (3, 5, 32), (100, 136, 96), (130, 300, 160), (64, 40, 224),
+                                   (257, 129, 4128), (200, 520, 288), (129, 257, 32)])
+def test_gemm_ragged_shapes(M, N, K):
+    """M, N off the 128/256 tiles and K off the 64/256 steps: the on-chip
+    padding must not change any written value, and nothing past N is written."""
+    rng = np.random.default_rng(M * 11 + N * 5 + K)
+    qa, sfa = _random_operand(M, K, rng)
+    qb, sfb = _random_operand(N, K, rng)
+    ga, gb = 1.25, 0.5
+    ref, dabs = O.gemm_f64(qa, sfa, ga, qb, sfb, gb, M, N, K)
+    for f32 in (True, False):
+        d, st = gemm(qa, sfa, ga, qb, sfb, gb, M, N, K, out_f32=f32)
+        assert st == 0
+        _check(d, ref, dabs, not f32, f"ragged {M}x{N}x{K}")
+
+
+def test_ragged_linear_layer_from_quantizers():
+    """Quantize X [200, 96] and W [136, 96] with the CUDA quantizers (whose
+    scale padding the GEMM relies on) and multiply: Y = X W^T."""
+    from gpu_helpers import quantize
+    x = synth.normal_bf16((200, 96), 51, 0, 1.0, 0.0, 0.01, 20.0)
+    w = synth.normal_bf16((136, 96), 51, 1, 0.02)
+    qa, sfa, ga, st_a = quantize(x)
+    qb, sfb, gb, st_b = quantize(w)
+    assert st_a == 0 and st_b == 0
+    ref, dabs = O.gemm_f64(qa, sfa, ga, qb, sfb, gb, 200, 136, 96)
+    d, st = gemm(qa, sfa, ga, qb, sfb, gb, 200, 136, 96, out_f32=True)
+    assert st == 0
+    _check(d, ref, dabs, False, "ragged layer")
+
+
 def test_scale_layout_one_hot():
     # Distinct power-of-two scale per (row, 16-block) of A: each output
     # element isolates one scale, so a wrong scale-factor layout shows up.

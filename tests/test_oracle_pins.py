@@ -470,3 +470,72 @@ def test_gemm_quantization_error_is_small():
     d, _ = O.gemm_f64(qa, sfa, ga, qb, sfb, gb, M, N, K)
     exact = synth.bf16_bits_to_f32(a).astype(np.float64) @ synth.bf16_bits_to_f32(b).astype(np.float64).T
     assert np.abs(d - exact).max() / np.abs(exact).max() < 0.2
+
+
+# ------------------------------------------------ quantization-noise meter ----
+# "FP4 All the Way", section "Describir": quantized training loses efficiency
+# once the gradient norm falls below about sqrt(3) times the quantization
+# noise.  The meter returns (sum (Q(x) - x)^2, sum x^2).
+
+_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_noise_meter_worked_example_E1():
+    """Hand-computed from E1's printed codes, scale byte 0x7E (448) and g: the
+    meter must sum the squared differences element by element."""
+    e = GOLD["E1"]
+    x = _bf16(e["x"]).reshape(1, 16)
+    q = np.frombuffer(bytes.fromhex(e["packed_hex"]), np.uint8).reshape(1, 8)
+    sf = np.zeros(O.sf_bytes(1, 16), np.uint8)
+    sf[0] = int(e["scale_byte"], 16)
+    g = float(np.uint32(int(e["g_f32_hex"], 16)).view(np.float32))
+    xs = synth.bf16_bits_to_f32(x[0]).astype(np.float64)
+    expect_e = expect_x = 0.0
+    for j, c in enumerate(e["codes"]):
+        c = int(c, 16)
+        val = (-1.0 if c & 8 else 1.0) * _E2M1[c & 7] * 448.0 * g
+        expect_e += (val - xs[j]) ** 2
+        expect_x += xs[j] ** 2
+    se, sx = O.quant_noise(x, q, sf, g)
+    assert se == pytest.approx(expect_e, rel=1e-12)
+    assert sx == pytest.approx(expect_x, rel=1e-12)
+    # by hand, with 448 g taken as 1: 0.10009765625^2 + 0.2001953125^2
+    # + 0.19921875^2 (0.3 -> 0.5) + 4 * 0.25^2 (0.75, 1.25, -1.75, 0.25 ties)
+    # + 2 * 0.5^2 (2.5, 3.5 ties) + 1 (5 -> 4) = 1.8397858142...
+    assert se == pytest.approx(1.839785814285278, rel=1e-6)
+
+
+def test_noise_meter_zero_on_representable_tensor():
+    """x = E2M1 value * 0.875 with amax 5.25: s_enc = 512, g = 2^-9 and every
+    block scale 448 are exact, so Q(x) = x and the noise is exactly 0."""
+    vals = np.array([v * 0.875 for v in _E2M1] + [-v * 0.875 for v in _E2M1], np.float32)
+    rng = np.random.default_rng(3)
+    x = rng.choice(vals, size=(32, 64)).astype(np.float32)
+    x[:, ::16] = 5.25  # every block holds the tensor max
+    xb = synth.f32_to_bf16_bits(x)
+    q, sf, g = O.quantize(xb)
+    assert g == 2.0 ** -9
+    se, sx = O.quant_noise(xb, q, sf, g)
+    assert se == 0.0
+    assert sx == pytest.approx(float((x.astype(np.float64) ** 2).sum()), rel=1e-15)
+
+
+def test_noise_meter_power_of_two_equivariance_and_rn_below_sr():
+    """Scaling x by 2^k scales Q(x) - x by 2^k exactly (tensor scale, block
+    scales and codes are unchanged), so both sums scale by 4^k exactly; and
+    nearest rounding never has more noise than stochastic rounding on the same
+    block scales."""
+    x = synth.normal_bf16((48, 80), 9, 0, 1.0, 0.0, 0.01, 30.0)
+    xf = synth.bf16_bits_to_f32(x)
+    q, sf, g = O.quantize(x, O.RN)
+    base = O.quant_noise(x, q, sf, g)
+    for k in (-6, 3):
+        xk = synth.f32_to_bf16_bits(xf * np.float32(2.0 ** k))
+        qk, sfk, gk = O.quantize(xk, O.RN)
+        sk = O.quant_noise(xk, qk, sfk, gk)
+        assert sk[0] == base[0] * 4.0 ** k and sk[1] == base[1] * 4.0 ** k
+    qs, sfs, gs = O.quantize(x, O.SR, 5)
+    assert np.array_equal(sfs, sf) and gs == g
+    assert O.quant_noise(x, qs, sfs, gs)[0] > base[0]
+    # NVFP4 of N(0,1) data: ||x|| / ||Q(x) - x|| is well above sqrt(3)
+    assert math.sqrt(base[1] / base[0]) > 5.0
