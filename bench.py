@@ -436,7 +436,8 @@ def _event_ms(fn, stream, reps=10, warmup=3):
 def measure_extras(step, stream, pk):
     """Kernels beside the step, each timed alone (not part of `value`):
     the quantization-noise meter on H's forward form, a GEMM with ragged
-    M, N, K, and cuBLAS bf16 matmul on the step's six GEMM shapes for context."""
+    M, N, K, the MXFP4 quantizer and GEMM (the comparison format), and cuBLAS
+    bf16 matmul on the step's six GEMM shapes for context."""
     import torch
 
     nv = step.nv
@@ -463,6 +464,25 @@ def measure_extras(step, stream, pk):
     tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
     out[f"gemm_ragged[{M}x{N}x{K}]"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1)}
     del a, b, sfa, sfb, d
+    # MXFP4 comparison format: one streaming quantizer pass over H, and the
+    # up-projection Fprop GEMM on MXFP4 operands of X and W_up
+    mq = torch.empty((T, F // 2), dtype=torch.uint8, device=dev)
+    msf = torch.empty((nv.nvfp4_sf_bytes(T, F),), dtype=torch.uint8, device=dev)
+    ms = _event_ms(lambda: nv.nvfp4_mxfp4_quantize(step.H, T, F, F, mq, msf, step.ws), stream)
+    byts = (2.0 + 0.5 + 1.0 / 32) * T * F
+    out["mxfp4_quantize[8192x11008]"] = {"ms": round(ms, 4), "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
+                                         "frac": round(byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3)}
+    xa = (torch.empty((T, D // 2), dtype=torch.uint8, device=dev),
+          torch.empty((nv.nvfp4_sf_bytes(T, D),), dtype=torch.uint8, device=dev))
+    wb = (torch.empty((F, D // 2), dtype=torch.uint8, device=dev),
+          torch.empty((nv.nvfp4_sf_bytes(F, D),), dtype=torch.uint8, device=dev))
+    nv.nvfp4_mxfp4_quantize(step.d_in[0]["X"], T, D, D, xa[0], xa[1], step.ws)
+    nv.nvfp4_mxfp4_quantize(step.d_in[0]["W_up"], F, D, D, wb[0], wb[1], step.ws)
+    ms = _event_ms(lambda: nv.nvfp4_mxfp4_gemm(xa[0], xa[1], wb[0], wb[1], T, F, D, step.H, F, nv.OUT_BF16,
+                                               step.ws), stream)
+    out["mxfp4_gemm[8192x11008x4096]"] = {"ms": round(ms, 4),
+                                           "TFLOP/s": round(GEMM_FLOPS / (ms * 1e-3) / 1e12, 1)}
+    del mq, msf, xa, wb
     # cuBLAS bf16 on the same six GEMMs (context: the unquantized layer)
     shapes = [(T, F, D), (T, D, F), (T, F, D), (D, F, T), (T, D, F), (F, D, T)]
     tot = 0.0

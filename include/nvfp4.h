@@ -204,6 +204,41 @@ nvfp4_status nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga,
                         void* d, int64_t ldd, nvfp4_out_dtype out_dtype,
                         void* ws, nvfp4_stream_t stream);
 
+/*
+ * MXFP4, the comparison format ["I ricercatori di Nvidia sbloccano ...",
+ * section "Come funziona NVFP4?": MXFP4 reached the same accuracy only with
+ * markedly more training data].  The pages do not define it; this follows the
+ * OCP Microscaling (MX) v1.0 specification: blocks of 32 contiguous
+ * elements, E2M1 codes, one UE8M0 scale 2^e per block, no tensor scale.
+ *   e = floor(log2(max |x| over the block)) - 2, clamped to [-127, 127]
+ *       (max 0 or below the smallest normal binary32: e = -127);
+ *   code = E2M1 round-to-nearest-even of x / 2^e, saturating at 6, sign kept;
+ *   scale byte = e + 127; a block holding Inf/NaN gets 0xFF (UE8M0 NaN),
+ *   zero codes, and NVFP4_ERR_NONFINITE is recorded in `ws`.
+ *   x   bf16 [rows, cols], leading dimension ld; cols % 32 == 0
+ *   q   out: uint8 [rows, cols/2] codes (element 2i in the low nibble)
+ *   sf  out: nvfp4_sf_bytes(rows, cols) bytes: one 32-bit word per row per 64
+ *       elements in the 128 x 4 atom layout, the two block scales in bytes 0
+ *       and 1, bytes 2 and 3 zero; byte of (row r, block kb) at
+ *       ((r/128) * Cp + kb/2) * 512 + (r%32) * 16 + ((r%128)/32) * 4 + kb%2,
+ *       Cp = ceil(cols / 64); padding rows and bytes are written as 0.
+ * One streaming pass (no tensor amax, no grid barrier).
+ */
+nvfp4_status nvfp4_mxfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                  uint8_t* q, uint8_t* sf, void* ws, nvfp4_stream_t stream);
+
+/*
+ * MXFP4 block-scaled matmul on the tcgen05 tensor cores (UE8M0 block-32
+ * scales): D[m, n] = sum_k A(m, k) B(n, k), A and B decoded MXFP4, binary32
+ * accumulation, output bf16 (nearest) or binary32.  Operands as
+ * nvfp4_mxfp4_quantize writes them, K contiguous; shapes and output rules as
+ * nvfp4_gemm (any M, N > 0, K % 32 == 0, only rows < M and columns < N
+ * written).  Padding scale bytes must not be 0xFF.
+ */
+nvfp4_status nvfp4_mxfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
+                              int64_t M, int64_t N, int64_t K, void* d, int64_t ldd,
+                              nvfp4_out_dtype out_dtype, void* ws, nvfp4_stream_t stream);
+
 /* Synchronise `stream` and return the sticky device status kept in `ws`
  * (NVFP4_OK if no device-side error was recorded). */
 nvfp4_status nvfp4_device_status(void* ws, nvfp4_stream_t stream);

@@ -25,7 +25,8 @@ STATUS = {0: "OK", 1: "ERR_ARG", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_NONFINI
 
 EXPORTS = ["nvfp4_sf_bytes", "nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_quantize",
            "nvfp4_quantize_2d", "nvfp4_rht_quantize", "nvfp4_quantize_dual", "nvfp4_quant_noise", "nvfp4_gemm",
-           "nvfp4_device_status", "nvfp4_status_str", "nvfp4_encode_probe", "nvfp4_quantize_noalloc"]
+           "nvfp4_mxfp4_quantize", "nvfp4_mxfp4_gemm", "nvfp4_device_status", "nvfp4_status_str",
+           "nvfp4_encode_probe", "nvfp4_quantize_noalloc"]
 
 
 class NVFP4Error(RuntimeError):
@@ -57,6 +58,8 @@ def load() -> ctypes.CDLL:
         "nvfp4_quantize_dual": ([p, i64, i64, i64, i32, u64, p, p, p, u64, i32, u64, p, p, p, p, p], i32),
         "nvfp4_quant_noise": ([p, i64, i64, i64, p, p, p, p, p], i32),
         "nvfp4_gemm": ([p, p, p, p, p, p, i64, i64, i64, p, i64, i32, p, p], i32),
+        "nvfp4_mxfp4_quantize": ([p, i64, i64, i64, p, p, p, p], i32),
+        "nvfp4_mxfp4_gemm": ([p, p, p, p, i64, i64, i64, p, i64, i32, p, p], i32),
         "nvfp4_device_status": ([p, p], i32),
         "nvfp4_status_str": ([i32], ctypes.c_char_p),
         "nvfp4_encode_probe": ([p, p, i64, p, p, p, p], i32),
@@ -121,6 +124,16 @@ def nvfp4_rht_quantize(x, T, C, ld, rht_seed, mode, sr_seed, qT, sfT, g_dec, ws,
     _check("nvfp4_rht_quantize", load().nvfp4_rht_quantize(
         _ptr(x), T, C, ld, rht_seed, mode, sr_seed, _ptr(qT), _ptr(sfT), _ptr(g_dec), _ptr(ws),
         _stream(stream)))
+
+
+def nvfp4_mxfp4_quantize(x, rows, cols, ld, q, sf, ws, stream=None) -> None:
+    _check("nvfp4_mxfp4_quantize", load().nvfp4_mxfp4_quantize(
+        _ptr(x), rows, cols, ld, _ptr(q), _ptr(sf), _ptr(ws), _stream(stream)))
+
+
+def nvfp4_mxfp4_gemm(a, sfa, b, sfb, M, N, K, d, ldd, out_dtype, ws, stream=None) -> None:
+    _check("nvfp4_mxfp4_gemm", load().nvfp4_mxfp4_gemm(
+        _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), M, N, K, _ptr(d), ldd, out_dtype, _ptr(ws), _stream(stream)))
 
 
 def nvfp4_quant_noise(x, rows, cols, ld, q, sf, g_dec, sums, stream=None) -> None:

@@ -293,8 +293,42 @@ nvfp4_status nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, c
     nvfp4_status st = check_device();
     if (st != NVFP4_OK)
         return st;
-    return launch_gemm(a, sfa, ga, b, sfb, gb, M, N, K, d, ldd, out_dtype, static_cast<Workspace*>(ws),
+    return launch_gemm(a, sfa, ga, b, sfb, gb, M, N, K, d, ldd, out_dtype, false, static_cast<Workspace*>(ws),
                        (cudaStream_t)stream);
+}
+
+nvfp4_status nvfp4_mxfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q, uint8_t* sf,
+                                  void* ws, nvfp4_stream_t stream)
+{
+    if (!x || !q || !sf || !ws)
+        return NVFP4_ERR_ARG;
+    if (rows <= 0 || cols <= 0 || cols % 32 != 0 || ld < cols || rows > (1ll << 31) || cols > (1ll << 31))
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sf) || !aligned16(ws) || ld % 8 != 0)
+        return NVFP4_ERR_ALIGN;
+    nvfp4_status st = check_device();
+    if (st != NVFP4_OK)
+        return st;
+    return launch_mxfp4_quantize(x, rows, cols, ld, q, sf, static_cast<Workspace*>(ws), (cudaStream_t)stream);
+}
+
+nvfp4_status nvfp4_mxfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb, int64_t M,
+                              int64_t N, int64_t K, void* d, int64_t ldd, nvfp4_out_dtype out_dtype, void* ws,
+                              nvfp4_stream_t stream)
+{
+    if (!a || !sfa || !b || !sfb || !d || !ws || (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32))
+        return NVFP4_ERR_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || K % 32 != 0 || ldd < N || K / 2 >= (1ll << 32) || M > (1ll << 31) ||
+        N > (1ll << 31))
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d) || !aligned16(ws) ||
+        (ldd * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 16 != 0)
+        return NVFP4_ERR_ALIGN;
+    nvfp4_status st = check_device();
+    if (st != NVFP4_OK)
+        return st;
+    return launch_gemm(a, sfa, nullptr, b, sfb, nullptr, M, N, K, d, ldd, out_dtype, true,
+                       static_cast<Workspace*>(ws), (cudaStream_t)stream);
 }
 
 nvfp4_status nvfp4_device_status(void* ws, nvfp4_stream_t stream)

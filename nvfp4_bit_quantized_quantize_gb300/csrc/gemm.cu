@@ -62,9 +62,11 @@ constexpr int kStoreBufBytes = 1024;  // per epilogue warp: 32 rows x 32 bytes
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kEpilogueWarps * kStoreBufBytes + sizeof(GemmCtl);
 
 // Instruction descriptor for kind::mxf4nvf4: E2M1 A and B (format 1),
-// K-major both, N >> 3 at bit 17, E4M3 scales (bit 23 = 0), M >> 4 at bit 24,
-// scale-factor ids 0 (four scales per row per K = 64 step).
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// K-major both, N >> 3 at bit 17, scale type at bit 23 (0 = E4M3 for NVFP4's
+// block-16 scales, 1 = UE8M0 for MXFP4's block-32 scales), M >> 4 at bit 24,
+// scale-factor ids 0 (one 32-bit scale word per row per K = 64 step).
+constexpr uint32_t kIdescNvf4 = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdescMxf4 = kIdescNvf4 | (1u << 23);
 
 struct GemmArgs {
     const uint8_t* sfa;
@@ -76,6 +78,16 @@ struct GemmArgs {
     int32_t M, N, K;
     int32_t out_f32;
 };
+
+template <bool kMx>
+__device__ __forceinline__ void mma_step(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t sfa, uint32_t sfb,
+                                         uint32_t acc)
+{
+    if constexpr (kMx)
+        mma_mxf4(d, adesc, bdesc, kIdescMxf4, sfa, sfb, acc);
+    else
+        mma_nvf4(d, adesc, bdesc, kIdescNvf4, sfa, sfb, acc);
+}
 
 // A 32-row x `width`-column output chunk that crosses the M or N edge is
 // written with plain stores instead of a tensor store, so that nothing outside
@@ -91,6 +103,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// kMx = false: NVFP4 (E4M3 block-16 scales, D scaled by ga * gb);
+// kMx = true: MXFP4 (UE8M0 block-32 scales, no tensor scale).  The scale
+// buffers have the same shape in both: one 32-bit word per row per K = 64.
+template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                      const __grid_constant__ CUtensorMap tma_d, const GemmArgs args, Workspace* ws)
@@ -201,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (uint32_t j = 0; j < 4; ++j)
-                        mma_nvf4(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, kIdesc, sfa_t + 4 * j,
-                                 sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                        mma_step<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
+                                      sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
                 } else {
                     // last stage: K = 64 steps, the final one possibly half
                     // filled (codes past K read as zeros, their scales are the
@@ -214,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_cp_32x128b_x4(sfb_t + 8 * j + 4, sfb_desc + off + 128 + 32 * j);
                     }
                     for (uint32_t j = 0; j < kk; ++j)
-                        mma_nvf4(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, kIdesc, sfa_t + 4 * j,
-                                 sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                        mma_step<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
+                                      sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
                 }
                 tc_commit(&ctl->empty[s]);
                 if (++s == kStages) {
@@ -233,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------- epilogue ----
         const uint32_t q = warp & 3;             // tensor-memory lane quarter of this warp
         const uint32_t half = (warp - 2) >> 2;   // columns 128*half .. +127
-        const float alpha = __fmul_rn(*args.ga, *args.gb);
+        const float alpha = kMx ? 1.0f : __fmul_rn(*args.ga, *args.gb);
         uint32_t titer = 0;
         for (uint32_t t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++titer) {
             const uint32_t tm = t % tiles_m, tn = t / tiles_m;
@@ -346,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
                          const uint8_t* sfb, const float* gb, int64_t M, int64_t N, int64_t K, void* d,
-                         int64_t ldd, nvfp4_out_dtype dt, Workspace* ws, cudaStream_t stream)
+                         int64_t ldd, nvfp4_out_dtype dt, bool mx, Workspace* ws, cudaStream_t stream)
 {
     CUtensorMap ma, mb;
     if (!encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(K / 2),
@@ -362,21 +378,24 @@ nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, 
                               (uint64_t)N, (uint64_t)M, (uint64_t)ldd * (f32 ? 4u : 2u), f32 ? 8u : 16u, 32u,
                               CU_TENSOR_MAP_SWIZZLE_NONE))
         return NVFP4_ERR_CUDA;
-    static bool attr_set[64] = {};
+    static bool attr_set[2][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return NVFP4_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(nvf4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess)
+    const void* kern = mx ? (const void*)nvf4_gemm_kernel<true> : (const void*)nvf4_gemm_kernel<false>;
+    if (dev < 64 && !attr_set[mx][dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
             return NVFP4_ERR_CUDA;
-        attr_set[dev] = true;
+        attr_set[mx][dev] = true;
     }
     GemmArgs args{sfa, sfb, ga, gb, d, ldd, (int32_t)M, (int32_t)N, (int32_t)K, dt == NVFP4_OUT_F32 ? 1 : 0};
     const int64_t ntiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int sms = device_sm_count();
     const int grid = (int)(ntiles < sms ? ntiles : sms);
-    nvf4_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, md, args, ws);
+    if (mx)
+        nvf4_gemm_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, md, args, ws);
+    else
+        nvf4_gemm_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, md, args, ws);
     return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 

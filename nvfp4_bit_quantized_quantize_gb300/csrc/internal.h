@@ -47,14 +47,17 @@ struct QuantParams {
 
 enum class QuantKind { k1x16, k2d, kRht, kDual };
 
-// Host launchers (quantize.cu, gemm.cu, noise.cu, probe.cu).  They assume the
+// Host launchers (quantize.cu, gemm.cu, noise.cu, mxfp4.cu, probe.cu).  They assume the
 // arguments were validated by the C-ABI layer.
 nvfp4_status launch_quantize(QuantKind kind, const void* x, int64_t ld, const QuantParams& p, Workspace* ws,
                              cudaStream_t stream);
 
 nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
                          const uint8_t* sfb, const float* gb, int64_t M, int64_t N, int64_t K, void* d,
-                         int64_t ldd, nvfp4_out_dtype dt, Workspace* ws, cudaStream_t stream);
+                         int64_t ldd, nvfp4_out_dtype dt, bool mx, Workspace* ws, cudaStream_t stream);
+
+nvfp4_status launch_mxfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q, uint8_t* sf,
+                                   Workspace* ws, cudaStream_t stream);
 
 nvfp4_status launch_quant_noise(const void* x, int64_t rows, int64_t cols, int64_t ld, const uint8_t* q,
                                 const uint8_t* sf, const float* g_dec, double* sums, cudaStream_t stream);

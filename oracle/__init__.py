@@ -87,6 +87,16 @@ def lib() -> ctypes.CDLL:
         L.or_gemm_f64_sampled.restype = None
         L.or_quant_noise.argtypes = [p, i64, i64, i64, p, p, ctypes.c_float, p]
         L.or_quant_noise.restype = None
+        L.or_e8m0_value.argtypes = [ctypes.c_int]
+        L.or_e8m0_value.restype = ctypes.c_double
+        L.or_mx_sf_offset.argtypes = [i64, i64, i64]
+        L.or_mx_sf_offset.restype = ctypes.c_size_t
+        L.or_mx_quantize.argtypes = [p, i64, i64, i64, p, p]
+        L.or_mx_quantize.restype = ctypes.c_int
+        L.or_mx_dequantize.argtypes = [p, p, i64, i64, p]
+        L.or_mx_dequantize.restype = None
+        L.or_mx_gemm_f64_sampled.argtypes = [p, p, p, p, i64, p, p, i64, p, p]
+        L.or_mx_gemm_f64_sampled.restype = None
         L.or_e2m1_rn_many.argtypes = [p, i64, p]
         L.or_e2m1_sr_many.argtypes = [p, p, i64, p]
         L.or_e4m3_rn_sat_many.argtypes = [p, i64, p]
@@ -268,3 +278,50 @@ def quant_noise(x_bf16: np.ndarray, q: np.ndarray, sf: np.ndarray, g: float):
     out = np.zeros(2, np.float64)
     lib().or_quant_noise(_ptr(x), R, C, C, _ptr(q), _ptr(sf), g, _ptr(out))
     return float(out[0]), float(out[1])
+
+
+# ----------------------------------------------------------------- MXFP4 ----
+
+def e8m0_value(code: int) -> float:
+    return float(lib().or_e8m0_value(int(code)))
+
+
+def mx_sf_offset(r: int, kb: int, kblocks: int) -> int:
+    return int(lib().or_mx_sf_offset(r, kb, kblocks))
+
+
+def mx_quantize(x_bf16: np.ndarray):
+    """MXFP4 (OCP MX v1.0) of a row-major bf16 matrix: (codes, scale bytes)."""
+    x = _c(x_bf16, np.uint16)
+    R, C = x.shape
+    q = np.empty((R, C // 2), np.uint8)
+    sf = np.empty(sf_bytes(R, C), np.uint8)
+    st = lib().or_mx_quantize(_ptr(x), R, C, C, _ptr(q), _ptr(sf))
+    if st != OK:
+        raise OracleError(st)
+    return q, sf
+
+
+def mx_dequantize(q: np.ndarray, sf: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    q, sf = _c(q, np.uint8), _c(sf, np.uint8)
+    out = np.empty((rows, cols), np.float64)
+    lib().or_mx_dequantize(_ptr(q), _ptr(sf), rows, cols, _ptr(out))
+    return out
+
+
+def mx_gemm_f64_sampled(a, sfa, b, sfb, K, ms, ns):
+    a, sfa, b, sfb = (_c(t, np.uint8) for t in (a, sfa, b, sfb))
+    ms = _c(ms, np.int64)
+    ns = _c(ns, np.int64)
+    d = np.empty(ms.size, np.float64)
+    dabs = np.empty(ms.size, np.float64)
+    lib().or_mx_gemm_f64_sampled(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), K, _ptr(ms), _ptr(ns), ms.size,
+                                 _ptr(d), _ptr(dabs))
+    return d, dabs
+
+
+def mx_gemm_f64(a, sfa, b, sfb, M, N, K):
+    """Full D = A B^T of two MXFP4 operands (binary64), with the |.| sums."""
+    mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    d, dabs = mx_gemm_f64_sampled(a, sfa, b, sfb, K, mm.ravel(), nn.ravel())
+    return d.reshape(M, N), dabs.reshape(M, N)

@@ -561,6 +561,110 @@ void or_quant_noise(const uint16_t* x, int64_t R, int64_t C, int64_t ld, const u
     sums[1] = sx;
 }
 
+/* ------------------------------------------------------------------------ */
+/* MXFP4, the comparison format [P3 "Come funziona NVFP4?": MXFP4 needed     */
+/* markedly more data for the same accuracy].  The pages do not define it;   */
+/* this restates the OCP Microscaling (MX) v1.0 conversion: 32-element       */
+/* blocks, E2M1 elements, one UE8M0 scale X = 2^e per block with             */
+/* e = floor(log2(max|V|)) - emax(E2M1) = floor(log2(max|V|)) - 2, clamped   */
+/* to the UE8M0 range; elements = E2M1 nearest-even of V / X, saturating.    */
+/* Readings: a block max of 0 (or below the smallest normal binary32, whose  */
+/* log2 floor lies under the range) takes e = -127; a block holding Inf/NaN  */
+/* takes the UE8M0 NaN byte 0xFF with zero codes and the call reports        */
+/* non-finite input.  Scale storage: one 32-bit word per row per 64          */
+/* elements in the 128 x 4 atom layout, block scales in bytes 0 and 1.       */
+/* ------------------------------------------------------------------------ */
+
+double or_e8m0_value(int code)
+{
+    if (code == 255)
+        return NAN;
+    return ldexp(1.0, code - 127);
+}
+
+size_t or_mx_sf_offset(int64_t r, int64_t kb, int64_t kblocks)
+{
+    int64_t steps = (kblocks + 1) / 2; /* 64-element steps per row */
+    return (size_t)(((r / 128) * steps + kb / 2) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + kb % 2);
+}
+
+int or_mx_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, uint8_t* q, uint8_t* sf)
+{
+    if (R <= 0 || C <= 0 || C % 32 != 0)
+        return OR_ERR_SHAPE;
+    int status = OR_OK;
+    int64_t kblocks = C / 32;
+    memset(sf, 0, or_sf_bytes(R, C));
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t kb = 0; kb < kblocks; ++kb) {
+            double amax = 0.0;
+            int finite = 1;
+            for (int j = 0; j < 32; ++j) {
+                float v = bf16_to_f32(x[r * ld + kb * 32 + j]);
+                if (!isfinite(v))
+                    finite = 0;
+                else if (fabs((double)v) > amax)
+                    amax = fabs((double)v);
+            }
+            size_t so = or_mx_sf_offset(r, kb, kblocks);
+            if (!finite) {
+                status = OR_ERR_NONFINITE;
+                sf[so] = 0xFF;
+                for (int j = 0; j < 32; ++j)
+                    put_code(q, C / 2, r, kb * 32 + j, 0);
+                continue;
+            }
+            int e = -127;
+            if (amax >= (double)FLT_MIN) {
+                int ex;
+                frexp(amax, &ex); /* amax = m 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1 */
+                e = (ex - 1) - 2;
+                if (e < -127)
+                    e = -127;
+                if (e > 127)
+                    e = 127;
+            }
+            sf[so] = (uint8_t)(e + 127);
+            for (int j = 0; j < 32; ++j) {
+                double v = (double)bf16_to_f32(x[r * ld + kb * 32 + j]);
+                put_code(q, C / 2, r, kb * 32 + j, or_e2m1_rn((float)ldexp(v, -e)));
+            }
+        }
+    return status;
+}
+
+static double mx_deq(const uint8_t* q, const uint8_t* sf, int64_t r, int64_t c, int64_t C)
+{
+    uint8_t byte = q[r * (C / 2) + c / 2];
+    int code = (c & 1) ? (byte >> 4) : (byte & 15);
+    return (double)or_e2m1_value(code) * or_e8m0_value(sf[or_mx_sf_offset(r, c / 32, C / 32)]);
+}
+
+void or_mx_dequantize(const uint8_t* q, const uint8_t* sf, int64_t R, int64_t C, double* out)
+{
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c)
+            out[r * C + c] = mx_deq(q, sf, r, c, C);
+}
+
+/* D[m][n] = sum_k deqA[m][k] deqB[n][k] (no tensor scale), binary64; dabs as
+ * for or_gemm_f64.  Evaluated at the listed (m, n) pairs. */
+void or_mx_gemm_f64_sampled(const uint8_t* a, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
+                            int64_t K, const int64_t* ms, const int64_t* ns, int64_t count,
+                            double* d, double* dabs)
+{
+    for (int64_t i = 0; i < count; ++i) {
+        double s = 0.0, sa = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = mx_deq(a, sfa, ms[i], k, K) * mx_deq(b, sfb, ns[i], k, K);
+            s += p;
+            sa += fabs(p);
+        }
+        d[i] = s;
+        dabs[i] = sa;
+    }
+}
+
 /* Batch helpers so tests can sweep the element codecs without a Python loop. */
 void or_e2m1_rn_many(const float* v, int64_t n, uint8_t* out)
 {

@@ -110,3 +110,30 @@ def quant_noise(x_bits, q, sf, g, ld=None):
     torch.cuda.synchronize()
     s = sums.cpu().numpy()
     return float(s[0]), float(s[1])
+
+
+def mx_quantize(x_bits, ld=None, ws=None):
+    rows, cols = x_bits.shape
+    x = dev_bf16(x_bits, ld)
+    q = torch.full((rows, cols // 2), 0xEE, dtype=torch.uint8, device="cuda")
+    sf = torch.full((nv.nvfp4_sf_bytes(rows, cols),), 0xEE, dtype=torch.uint8, device="cuda")
+    ws = nv.alloc_workspace() if ws is None else ws
+    nv.nvfp4_mxfp4_quantize(x, rows, cols, x.shape[1], q, sf, ws)
+    st = nv.nvfp4_device_status(ws)
+    return q.cpu().numpy(), sf.cpu().numpy(), st
+
+
+def mx_gemm(qa, sfa, qb, sfb, M, N, K, out_f32=False, ws=None):
+    """MXFP4 GEMM with the same NaN-filled, padded output check as gemm()."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    unit = 4 if out_f32 else 8
+    ldd = ((N + unit - 1) // unit) * unit
+    d = torch.full((M + 32, ldd), float("nan"), dtype=torch.float32 if out_f32 else torch.bfloat16,
+                   device="cuda")
+    ws = nv.alloc_workspace() if ws is None else ws
+    nv.nvfp4_mxfp4_gemm(t(qa), t(sfa), t(qb), t(sfb), M, N, K, d, ldd, nv.OUT_F32 if out_f32 else nv.OUT_BF16, ws)
+    st = nv.nvfp4_device_status(ws)
+    out = d.float().cpu().numpy().astype(np.float64)
+    assert np.isnan(out[:M, N:]).all(), "GEMM wrote past column N"
+    assert np.isnan(out[M:]).all(), "GEMM wrote past row M"
+    return np.ascontiguousarray(out[:M, :N]), st

@@ -1,0 +1,156 @@
+"""MXFP4 (the comparison format; OCP Microscaling v1.0 conversion) on the GPU:
+the quantizer bit for bit against the oracle, the block-scaled GEMM within the
+same tolerance as the NVFP4 GEMM (1e-5 * sum|a*b| for binary32 output, plus
+one bf16 rounding for bf16 output)."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import nvfp4_bit_quantized_quantize_gb300 as nv
+from nvfp4_bit_quantized_quantize_gb300 import synth
+
+from gpu_helpers import mx_gemm, mx_quantize
+
+pytestmark = pytest.mark.gpu
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")))
+REL = 1e-5
+BF16_REL = 2.0 ** -8
+
+
+def _same(g, r, what):
+    bad = np.flatnonzero(np.asarray(g).ravel() != np.asarray(r).ravel())
+    assert bad.size == 0, f"{what}: {bad.size} mismatches, first {bad[:8]}"
+
+
+def _check(d, ref, dabs, bf16, what):
+    tol = REL * dabs + (BF16_REL * np.abs(ref) if bf16 else 0.0)
+    bad = np.flatnonzero((np.abs(d - ref) > tol).ravel())
+    assert bad.size == 0, f"{what}: {bad.size} out of tolerance, first {bad[:5]}"
+
+
+@pytest.mark.parametrize("shape", [(1, 32), (48, 96), (200, 1056), (130, 64), (1024, 4096), (257, 160)])
+def test_mx_quantize_parity(shape):
+    x = synth.normal_bf16(shape, 71, shape[0] % 5, 1.0, 0.0, 0.01, 1e4)
+    q, sf, st = mx_quantize(x)
+    rq, rsf = O.mx_quantize(x)
+    assert st == 0
+    _same(q, rq, "codes")
+    _same(sf, rsf, "scales (with padding)")
+
+
+def test_mx_quantize_worked_example_and_leading_dimension():
+    e = GOLD["MX1"]
+    x = np.zeros(128, np.float32)
+    for b, blk in enumerate(e["blocks"]):
+        for j, v in enumerate(blk["x"]):
+            x[b * 32 + j] = float(v)
+    xb = synth.f32_to_bf16_bits(x).reshape(1, 128)
+    q, sf, st = mx_quantize(xb, ld=136)
+    assert st == 0
+    for b, blk in enumerate(e["blocks"]):
+        assert q[0, b * 16:b * 16 + 8].tobytes().hex() == blk["packed_hex_first8"]
+        assert sf[e["scale_offsets_row0"][b]] == int(blk["scale_byte"], 16)
+
+
+def test_mx_quantize_tiny_and_huge_blocks():
+    # subnormal, tiny-normal and near-bf16-max block maxima: scale byte 0 / clamp / top of range
+    vals = np.array([1e-40, 3e-38, 1e-30, 1.0, 3e38, -2.5e38], np.float32)
+    x = np.zeros((2, 192), np.float32)
+    for i, v in enumerate(vals):
+        x[i % 2, (i // 2) * 64 + 3] = v
+        x[i % 2, (i // 2) * 64 + 40] = v / 3
+    xb = synth.f32_to_bf16_bits(x)
+    q, sf, st = mx_quantize(xb)
+    rq, rsf = O.mx_quantize(xb)
+    assert st == 0
+    _same(q, rq, "codes")
+    _same(sf, rsf, "scales")
+
+
+def test_mx_nonfinite_block_gets_nan_scale():
+    x = synth.normal_bf16((64, 128), 72, 0, 1.0)
+    x[5, 70] = 0x7F80  # +Inf in row 5, block 2
+    q, sf, st = mx_quantize(x)
+    assert st == 4  # NVFP4_ERR_NONFINITE
+    assert sf[O.mx_sf_offset(5, 2, 4)] == 0xFF
+    assert not q[5, 32:48].any()
+    clean = x.copy()
+    clean[5, 64:96] = 0
+    rq, rsf = O.mx_quantize(clean)
+    keep = np.ones(q.shape, bool)
+    keep[5, 32:48] = False
+    _same(q[keep], rq[keep], "codes of the finite blocks")
+
+
+def _random_mx_operand(rows, K, rng):
+    q = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
+    sf = np.zeros(O.sf_bytes(rows, K), np.uint8)
+    kb = K // 32
+    for r in range(rows):
+        for k in range(kb):
+            sf[O.mx_sf_offset(r, k, kb)] = rng.integers(120, 135)
+    return q, sf
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 384, 320), (100, 136, 96), (3, 5, 32),
+                                   (130, 300, 4128), (512, 512, 1024)])
+def test_mx_gemm_parity(M, N, K):
+    rng = np.random.default_rng(M + 3 * N + 7 * K)
+    qa, sfa = _random_mx_operand(M, K, rng)
+    qb, sfb = _random_mx_operand(N, K, rng)
+    ref, dabs = O.mx_gemm_f64(qa, sfa, qb, sfb, M, N, K)
+    for f32 in (True, False):
+        d, st = mx_gemm(qa, sfa, qb, sfb, M, N, K, out_f32=f32)
+        assert st == 0
+        _check(d, ref, dabs, not f32, f"mx {M}x{N}x{K}")
+
+
+def test_mx_gemm_scale_layout_one_hot():
+    """A distinct power-of-two scale per (row, 32-block) of A and B rows that
+    each select one block: every output isolates one scale byte, so a wrong
+    reading of the scale words (bytes 0 and 1 per 64 elements) shows up."""
+    M, N, K = 128, 128, 256
+    kb = K // 32
+    rng = np.random.default_rng(9)
+    qa = np.full((M, K // 2), 0x22, np.uint8)  # all 1.0
+    qb = np.zeros((N, K // 2), np.uint8)
+    for n in range(N):
+        blk = n % kb
+        qb[n, blk * 16:(blk + 1) * 16] = 0x22
+    sfa = np.zeros(O.sf_bytes(M, K), np.uint8)
+    sfb = np.zeros(O.sf_bytes(N, K), np.uint8)
+    for r in range(M):
+        for k in range(kb):
+            sfa[O.mx_sf_offset(r, k, kb)] = rng.integers(110, 140)
+    for n in range(N):
+        for k in range(kb):
+            sfb[O.mx_sf_offset(n, k, kb)] = 127
+    ref, _ = O.mx_gemm_f64(qa, sfa, qb, sfb, M, N, K)
+    d, st = mx_gemm(qa, sfa, qb, sfb, M, N, K, out_f32=True)
+    assert st == 0
+    assert np.array_equal(d, ref)
+
+
+def test_mx_linear_layer_from_quantizers():
+    """MXFP4 Y = X W^T from the GPU quantizers against the oracle path, and
+    the same layer in NVFP4 for comparison: on N(0,1) activations with
+    outliers NVFP4 is the more accurate of the two (the pages' claim is about
+    training data needed; this checks only the per-layer error ordering)."""
+    x = synth.normal_bf16((256, 512), 73, 0, 1.0, 0.0, 0.001, 100.0)
+    w = synth.normal_bf16((384, 512), 73, 1, 0.02)
+    qa, sfa, st_a = mx_quantize(x)
+    qb, sfb, st_b = mx_quantize(w)
+    assert st_a == 0 and st_b == 0
+    ref, dabs = O.mx_gemm_f64(qa, sfa, qb, sfb, 256, 384, 512)
+    d, st = mx_gemm(qa, sfa, qb, sfb, 256, 384, 512, out_f32=True)
+    assert st == 0
+    _check(d, ref, dabs, False, "mx layer")
+    exact = synth.bf16_bits_to_f32(x).astype(np.float64) @ synth.bf16_bits_to_f32(w).astype(np.float64).T
+    na, nsa, ga = O.quantize(x)
+    nb, nsb, gb = O.quantize(w)
+    nref, _ = O.gemm_f64(na, nsa, ga, nb, nsb, gb, 256, 384, 512)
+    assert np.linalg.norm(nref - exact) < np.linalg.norm(ref - exact)

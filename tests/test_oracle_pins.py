@@ -539,3 +539,85 @@ def test_noise_meter_power_of_two_equivariance_and_rn_below_sr():
     assert O.quant_noise(x, qs, sfs, gs)[0] > base[0]
     # NVFP4 of N(0,1) data: ||x|| / ||Q(x) - x|| is well above sqrt(3)
     assert math.sqrt(base[1] / base[0]) > 5.0
+
+
+# ------------------------------------------------------------------ MXFP4 ----
+# The comparison format ("I ricercatori di Nvidia sbloccano ...", section
+# "Come funziona NVFP4?"); conversion per the OCP Microscaling v1.0 spec.
+
+def _mx_row_from_golden():
+    e = GOLD["MX1"]
+    x = np.zeros(128, np.float32)
+    for b, blk in enumerate(e["blocks"]):
+        for j, v in enumerate(blk["x"]):
+            x[b * 32 + j] = float(v)
+    return synth.f32_to_bf16_bits(x).reshape(1, 128), e
+
+
+def test_mx_worked_example():
+    x, e = _mx_row_from_golden()
+    q, sf = O.mx_quantize(x)
+    for b, blk in enumerate(e["blocks"]):
+        assert q[0, b * 16:b * 16 + 8].tobytes().hex() == blk["packed_hex_first8"], b
+        assert not q[0, b * 16 + 8:b * 16 + 16].any()
+        assert sf[e["scale_offsets_row0"][b]] == int(blk["scale_byte"], 16), b
+        assert O.mx_sf_offset(0, b, 4) == e["scale_offsets_row0"][b]
+    used = set(e["scale_offsets_row0"])
+    assert all(sf[i] == 0 for i in range(sf.size) if i not in used)  # padding
+    d = O.mx_dequantize(q, sf, 1, 128)
+    assert d[0, :7].tolist() == [6.0, -6.0, 1.0, 0.0, 4.0, 2.0, -0.0]
+    assert math.copysign(1.0, d[0, 6]) == -1.0
+    assert d[0, 32:35].tolist() == [0.75, 0.125, -0.25]
+    assert d[0, 96] == 384.0
+
+
+def test_mx_e8m0_and_layout():
+    assert O.e8m0_value(127) == 1.0 and O.e8m0_value(0) == 2.0 ** -127 and O.e8m0_value(254) == 2.0 ** 127
+    assert math.isnan(O.e8m0_value(255))
+    # 128-row x 4-word atoms, two block scales per word in bytes 0 and 1
+    offs = {O.mx_sf_offset(r, kb, 6) for r in range(256) for kb in range(6)}
+    assert len(offs) == 256 * 6 and max(offs) < O.sf_bytes(256, 192)
+    assert all(o % 4 in (0, 1) for o in offs)
+    assert O.mx_sf_offset(33, 3, 6) == (0 * 3 + 1) * 512 + 1 * 16 + 1 * 4 + 1
+    assert O.mx_sf_offset(130, 4, 6) == (1 * 3 + 2) * 512 + 2 * 16 + 0 * 4 + 0
+
+
+def test_mx_power_of_two_equivariance_and_error_bound():
+    """x -> 2^k x leaves the codes alone and adds k to every scale byte; every
+    element not saturated is within half an E2M1 step of its block grid."""
+    x = synth.normal_bf16((40, 96), 12, 0, 1.0, 0.0, 0.02, 40.0)
+    q, sf = O.mx_quantize(x)
+    xf = synth.bf16_bits_to_f32(x)
+    for k in (-9, 5):
+        qk, sfk = O.mx_quantize(synth.f32_to_bf16_bits(xf * np.float32(2.0 ** k)))
+        assert np.array_equal(qk, q)
+        used = np.array([O.mx_sf_offset(r, kb, 3) for r in range(40) for kb in range(3)])
+        assert np.array_equal(sfk[used].astype(int), sf[used].astype(int) + k)
+    d = O.mx_dequantize(q, sf, 40, 96)
+    for r in range(40):
+        for kb in range(3):
+            blk = xf[r, kb * 32:(kb + 1) * 32].astype(np.float64)
+            X = 2.0 ** math.floor(math.log2(np.abs(blk).max())) / 4.0
+            v = blk / X
+            got = d[r, kb * 32:(kb + 1) * 32]
+            step = np.where(np.abs(v) < 2, 0.5, np.where(np.abs(v) < 4, 1.0, 2.0)) * X
+            ok = np.abs(v) <= 6
+            assert np.all(np.abs(got - blk)[ok] <= step[ok] / 2 + 1e-30)
+            assert np.all(np.abs(got[~ok]) == 6 * X)
+
+
+def test_mx_gemm_brute_force_and_nonfinite():
+    M, N, K = 16, 24, 96
+    a = synth.normal_bf16((M, K), 13, 0, 1.0)
+    b = synth.normal_bf16((N, K), 13, 1, 0.02)
+    qa, sfa = O.mx_quantize(a)
+    qb, sfb = O.mx_quantize(b)
+    d, dabs = O.mx_gemm_f64(qa, sfa, qb, sfb, M, N, K)
+    A = O.mx_dequantize(qa, sfa, M, K)
+    B = O.mx_dequantize(qb, sfb, N, K)
+    assert np.allclose(d, A @ B.T, rtol=1e-12, atol=1e-15)
+    assert np.allclose(dabs, np.abs(A) @ np.abs(B).T, rtol=1e-12)
+    bad = a.copy()
+    bad[3, 40] = 0x7FC0  # NaN
+    with pytest.raises(O.OracleError):
+        O.mx_quantize(bad)
