@@ -276,6 +276,26 @@ def run_e2e(step, args, stream):
     return t0, t1, h2d, d2h
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: with N replicas the job ends when the last one
+    does.  One all-reduce MAX of a single float64 (on `device`: the rank's GPU
+    under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step_per_rank: float, ms_per_step: float) -> float:
+    """Whole-job throughput of N weak-scaled replicas: every rank does one
+    step's flops in the slowest rank's step time."""
+    return world * flops_per_step_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -319,11 +339,7 @@ def run_ours(args, rank, world, local_rank):
     t1.record(stream)
     barrier()
     clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
     st = step.nv.nvfp4_device_status(step.ws)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {step.nv.nvfp4_status_str(st)}")
@@ -334,7 +350,7 @@ def run_ours(args, rank, world, local_rank):
             per_kind.setdefault((kind, shape), []).append(a.elapsed_time(b))
     ms_step = ms_total / args.steps
     flops_step = N_GEMMS * GEMM_FLOPS
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = job_tflops(world, flops_step, ms_step)
 
     pk = peaks()
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
@@ -395,15 +411,11 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         e0, e1, h2d, d2h = run_e2e(step, args, stream)
         barrier()
-        ms_e2e = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, dev)
         st = step.nv.nvfp4_device_status(step.ws)
         if st != 0:
             raise RuntimeError(f"device status after end-to-end steps: {step.nv.nvfp4_status_str(st)}")
-        line["e2e"] = {"value": round(world * flops_step / (ms_e2e / args.steps * 1e-3) / 1e12, 2),
+        line["e2e"] = {"value": round(job_tflops(world, flops_step, ms_e2e / args.steps), 2),
                        "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": round(ms_e2e / args.steps, 4),
                        "note": "pinned host inputs copied in and results copied out every step; copies on "
