@@ -423,6 +423,7 @@ def run_ours(args, rank, world, local_rank):
 
     if not args.no_extras:
         line["extras"] = measure_extras(step, stream, pk)
+        line["configs"] = measure_configs(step, stream, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     return line
@@ -443,6 +444,94 @@ def _event_ms(fn, stream, reps=10, warmup=3):
     b.record(stream)
     torch.cuda.synchronize()
     return a.elapsed_time(b) / reps
+
+
+def _flushed_ms(fn, stream, flush, reps=20, warmup=5):
+    """Median CUDA-event time of fn() on `stream`, the L2 flushed (a buffer of
+    twice its size written) before every launch; the flush is outside the
+    events."""
+    import torch
+
+    evs = []
+    for i in range(warmup + reps):
+        flush.fill_(i)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        if i >= warmup:
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def measure_configs(step, stream, pk):
+    """The other workloads' kernels alone (5 warm-up launches, median of 20,
+    L2 flushed before each launch): the quantize sweep (1024^2, 4096^2,
+    8192^2, RN and SR), the 2-D weight Fprop (W 20480x5120 2-D with
+    transpose, X 8192x5120 RN, GEMM 8192x20480x5120) and the RHT+SR Wgrad
+    (dY and X 16384x5120, GEMM 5120x5120x16384).  Inputs are N(0,1)
+    (N(0,0.02) for W, N(0,1e-3) for dY) drawn on the device."""
+    import torch
+
+    nv = step.nv
+    dev = step.dev
+    ws = step.ws
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.int32, device=dev)
+    out = {}
+
+    def qline(kind, rows, cols, ms):
+        gbs = quant_bytes(kind, rows, cols) / (ms * 1e-3) / 1e9
+        return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 3)}
+
+    def gline(M, N, K, ms):
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / fp4_peak, 3)}
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    for n in (1024, 4096, 8192):
+        x = torch.randn((n, n), generator=gen, device=dev).to(torch.bfloat16)
+        q, sf, g = nv.alloc_quantized(n, n, dev)
+        for mode, tag in ((nv.RN, "rn"), (nv.SR, "sr")):
+            ms = _flushed_ms(lambda: nv.nvfp4_quantize(x, n, n, n, mode, 7, q, sf, g, ws), stream, flush)
+            out[f"quantize_sweep/quantize_1x16[{tag}x{n}x{n}]"] = qline("quantize_1x16", n, n, ms)
+        del x, q, sf, g
+    # 2-D weight Fprop
+    M, N, K = 8192, 20480, 5120
+    w = (torch.randn((N, K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+    x = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
+    wq, wqT, xq = nv.alloc_quantized(N, K, dev), nv.alloc_quantized(K, N, dev), nv.alloc_quantized(M, K, dev)
+    ms = _flushed_ms(lambda: nv.nvfp4_quantize_2d(w, N, K, K, wq[0], wq[1], wqT[0], wqT[1], wq[2], ws), stream,
+                     flush)
+    out[f"fprop_w2d/quantize_2d_t[{N}x{K}]"] = qline("quantize_2d_t", N, K, ms)
+    ms = _flushed_ms(lambda: nv.nvfp4_quantize(x, M, K, K, nv.RN, 0, *xq, ws), stream, flush)
+    out[f"fprop_w2d/quantize_1x16[rnx{M}x{K}]"] = qline("quantize_1x16", M, K, ms)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ms = _flushed_ms(lambda: nv.nvfp4_gemm(xq[0], xq[1], xq[2], wq[0], wq[1], wq[2], M, N, K, d, N,
+                                           nv.OUT_BF16, ws), stream, flush)
+    out[f"fprop_w2d/gemm[{M}x{N}x{K}]"] = gline(M, N, K, ms)
+    del w, x, wq, wqT, xq, d
+    # RHT + SR Wgrad
+    T, C = 16384, 5120
+    dy = (torch.randn((T, C), generator=gen, device=dev) * 1e-3).to(torch.bfloat16)
+    x = torch.randn((T, C), generator=gen, device=dev).to(torch.bfloat16)
+    dyT, xT = nv.alloc_quantized(C, T, dev), nv.alloc_quantized(C, T, dev)
+    ms = _flushed_ms(lambda: nv.nvfp4_rht_quantize(dy, T, C, C, 4, nv.SR, 3, *dyT, ws), stream, flush)
+    out[f"wgrad_rht_sr/rht_quantize[srx{T}x{C}]"] = qline("rht_quantize", T, C, ms)
+    ms = _flushed_ms(lambda: nv.nvfp4_rht_quantize(x, T, C, C, 4, nv.SR, 5, *xT, ws), stream, flush)
+    out[f"wgrad_rht_sr/rht_quantize[srx{T}x{C}]/X"] = qline("rht_quantize", T, C, ms)
+    d = torch.empty((C, C), dtype=torch.bfloat16, device=dev)
+    ms = _flushed_ms(lambda: nv.nvfp4_gemm(dyT[0], dyT[1], dyT[2], xT[0], xT[1], xT[2], C, C, T, d, C,
+                                           nv.OUT_BF16, ws), stream, flush)
+    out[f"wgrad_rht_sr/gemm[{C}x{C}x{T}]"] = gline(C, C, T, ms)
+    del dy, x, dyT, xT, d, flush
+    st = nv.nvfp4_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after config kernels: {nv.nvfp4_status_str(st)}")
+    return out
 
 
 def measure_extras(step, stream, pk):

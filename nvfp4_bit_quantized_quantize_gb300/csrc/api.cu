@@ -27,8 +27,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t dim0, uint64_t dim1,
-                          uint64_t stride1_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle)
+namespace {
+// cuTensorMapEncodeTiled, resolved once through the runtime (no libcuda link).
+EncodeTiledFn encode_fn()
 {
     static EncodeTiledFn fn = nullptr;
     if (fn == nullptr) {
@@ -37,15 +38,43 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* bas
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
                 cudaSuccess ||
             q != cudaDriverEntryPointSuccess || p == nullptr)
-            return false;
+            return nullptr;
         fn = reinterpret_cast<EncodeTiledFn>(p);
     }
+    return fn;
+}
+}  // namespace
+
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t dim0, uint64_t dim1,
+                          uint64_t stride1_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return false;
     const cuuint64_t dims[2] = {dim0, dim1};
     const cuuint64_t strides[1] = {stride1_bytes};
     const cuuint32_t box[2] = {box0, box1};
     const cuuint32_t elem_strides[2] = {1, 1};
     return fn(map, dtype, 2, base, dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_sf_atom_map(CUtensorMap* map, const uint8_t* sf, int64_t rows, int64_t K, uint32_t row_tiles_per_box)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    // 512-byte atoms as 64 x 8-byte elements; the atoms of one 128-row tile
+    // are contiguous along K; row tiles follow each other
+    const cuuint64_t cp = (cuuint64_t)((K / 16 + 3) / 4);
+    const cuuint64_t tiles = (cuuint64_t)((rows + 127) / 128);
+    const cuuint64_t dims[3] = {64, cp, tiles};
+    const cuuint64_t strides[2] = {512, cp * 512};
+    const cuuint32_t box[3] = {64, 4, row_tiles_per_box};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t*>(sf), dims, strides, box, elem_strides,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ----------------------------------------------------------------- probe ----

@@ -71,6 +71,12 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* bas
                           uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
                           CUtensorMapSwizzle swizzle);
 
+// Tensor map over a scale buffer in the 128 x 4 atom layout: a 3-D tensor of
+// 512-byte atoms (64 x 8-byte elements) x atoms along K x 128-row tiles; a
+// box is 4 atoms (one 256-element K stage) of `row_tiles_per_box` row tiles.
+// Atoms past K or past the last row tile read as zeros.
+bool encode_sf_atom_map(CUtensorMap* map, const uint8_t* sf, int64_t rows, int64_t K, uint32_t row_tiles_per_box);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
