@@ -90,71 +90,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Worksp
     }
 }
 
-// ------------------------------------------------------------- clusters ----
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Shared::cluster address of the object at CTA-local shared address `saddr`
-// in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
-// Arrive on an mbarrier of any CTA of the cluster, relaxed: for signals that
-// carry no data of the arriving thread (what they order was completed by an
-// earlier wait: a TMA completion, a tcgen05.wait::ld), so no fence is paid.
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n.reg .pred p;\n"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// mbar_wait for barriers that other CTAs of the cluster arrive on (acquire at
-// cluster scope); same bounds.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, Workspace* ws,
-                                                  volatile int* abort)
-{
-    if (mbar_try_wait_cluster(bar, parity))
-        return true;
-    const uint64_t t0 = global_ns();
-    while (true) {
-        if (mbar_try_wait_cluster(bar, parity))
-            return true;
-        if (abort && *abort)
-            return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            record_status(ws, NVFP4_ERR_TIMEOUT);
-            if (abort)
-                *abort = 1;
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // ------------------------------------------------------------------ TMA ----
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m)
 {
@@ -263,70 +198,6 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
-}
-
-// ---- paired-SM (cta_group::2) forms: one thread of the even CTA of a
-// two-CTA cluster issues for both; A rows and B rows are split between the
-// two CTAs' shared memory, each CTA's tensor memory holds its half of D.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols)
-{
-    // one warp of each of the two CTAs executes this collectively
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.block16 [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.block32 [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-// Each CTA of the pair copies the block at `sdesc` in its own shared memory
-// into its own tensor memory (replicated into the four lane quarters).
-__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// Arrive once on the mbarrier at this shared offset in every CTA of `mask`
-// when all prior tcgen05 work of this thread has completed.
-__device__ __forceinline__ void tc_commit_pair_multicast(uint64_t* bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_commit_pair(uint64_t* bar)
-{
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
 }
 
 // Copy a 32-row x 16-byte block of shared memory into tmem, replicated into

@@ -264,12 +264,8 @@ nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, 
     if (!encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(K / 2),
                               (uint64_t)M, (uint64_t)(K / 2), 128u, (uint32_t)BM, CU_TENSOR_MAP_SWIZZLE_128B))
         return NVFP4_ERR_CUDA;
-    // the paired-SM kernel is kept for study but not routed: measured slower
-    // (3.07 against 3.33 PFLOP/s on 8192 x 11008 x 4096)
-    const bool pair = false;
     if (!encode_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(b), (uint64_t)(K / 2),
-                              (uint64_t)N, (uint64_t)(K / 2), 128u, pair ? 128u : (uint32_t)BN,
-                              CU_TENSOR_MAP_SWIZZLE_128B))
+                              (uint64_t)N, (uint64_t)(K / 2), 128u, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return NVFP4_ERR_CUDA;
 
     CUtensorMap md;
@@ -279,8 +275,6 @@ nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, 
                               CU_TENSOR_MAP_SWIZZLE_NONE))
         return NVFP4_ERR_CUDA;
     GemmArgs args{sfa, sfb, ga, gb, d, ldd, (int32_t)M, (int32_t)N, (int32_t)K, dt == NVFP4_OUT_F32 ? 1 : 0};
-    if (pair)
-        return launch_gemm_pair(ma, mb, md, args, mx, ws, stream);
     CUtensorMap msfa, msfb;
     if (!encode_sf_atom_map(&msfa, sfa, M, K, 1) || !encode_sf_atom_map(&msfb, sfb, N, K, 2))
         return NVFP4_ERR_CUDA;

@@ -1,4 +1,5 @@
-// Pieces shared by the block-scaled GEMM kernels (one-CTA and paired-SM).
+// Pieces of the block-scaled GEMM kernel: arguments, instruction descriptor,
+// epilogue store.
 #pragma once
 
 #include "device.cuh"
@@ -122,9 +123,5 @@ __device__ __forceinline__ void epilogue_store(const uint32_t (&r)[4][32], float
         }
     }
 }
-
-// The paired-SM kernel (gemm_pair.cu); B's tensor map must have 128-row boxes.
-nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
-                              const GemmArgs& args, bool mx, Workspace* ws, cudaStream_t stream);
 
 }  // namespace nvfp4
