@@ -70,11 +70,25 @@ __device__ __forceinline__ void tile_coords(int64_t t, const QuantParams& p, int
 // writes 8 bytes of packed codes.  ftab holds rn(s_enc / E4M3value(b)) for the
 // 126 non-zero finite scale bytes: the same rounded quotient the definition
 // asks for, computed once per CTA instead of once per block.
+// rn(b / 6) in binary32.  For b >= 2^-124 the quotient rn(b * rn(1/6)),
+// corrected once with the exact fused-multiply-add residual, is the correctly
+// rounded quotient (checked exhaustively over every binary32 b in
+// [2^-124, FLT_MAX]); smaller b (subnormal quotients) take the division.
+__device__ __forceinline__ float div6_rn(float b)
+{
+    if (b >= 0x1p-124f) {
+        const float r6 = 0x1.555556p-3f;  // rn(1/6)
+        const float q0 = __fmul_rn(b, r6);
+        return __fmaf_rn(__fmaf_rn(-6.0f, q0, b), r6, q0);
+    }
+    return __fdiv_rn(b, 6.0f);
+}
+
 __device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], float bamax, float s_enc,
                                                   const float* ftab, int mode, uint64_t seed, uint64_t blk,
                                                   uint32_t& lo32, uint32_t& hi32)
 {
-    const uint32_t sb = e4m3_rn_sat(__fmul_rn(__fdiv_rn(bamax, 6.0f), s_enc));
+    const uint32_t sb = e4m3_rn_sat(__fmul_rn(div6_rn(bamax), s_enc));
     if (sb == 0) {  // the block decodes to zero: signed zeros
         lo32 = hi32 = 0;
 #pragma unroll
@@ -302,7 +316,9 @@ struct OpRht {
         tma_load_2d(dst + 8192, m, bar, (int32_t)(ct * 128 + 64), (int32_t)(tt * 64));
     }
 
-    // y = (1/4) H16 D v for this thread's channel and token block.
+    // y = (1/4) H16 D v for this thread's channel and token block (without
+    // the exact final 1/4 when kQuarter is false).
+    template <bool kQuarter = true>
     __device__ static void transform(const uint8_t* tile, int ctid, uint32_t signs, float (&y)[16])
     {
         const int lane = ctid & 31, cw = ctid >> 5;
@@ -326,20 +342,24 @@ struct OpRht {
                 y[i + hs] = __fsub_rn(a, b);
             }
         }
+        if constexpr (kQuarter) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            y[i] = __fmul_rn(y[i], 0.25f);
+            for (int i = 0; i < 16; ++i)
+                y[i] = __fmul_rn(y[i], 0.25f);
+        }
     }
 
+    // max |y| as float bits (NaN-propagating).  Multiplying by 1/4 is exact
+    // and monotone, so max |H16 D v| / 4 equals the max over the scaled values.
     __device__ static uint32_t transformed_amax(const uint8_t* tile, int ctid, const QuantParams& p)
     {
-        float y[16];
-        transform(tile, ctid, p.rht_signs, y);
-        uint32_t m = 0;
+        float u[16];
+        transform<false>(tile, ctid, p.rht_signs, u);
+        float m = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            m = max(m, __float_as_uint(y[i]) & 0x7FFFFFFFu);
-        return m;
+            asm("max.NaN.f32 %0, %1, %2;" : "=f"(m) : "f"(m), "f"(fabsf(u[i])));
+        return __float_as_uint(__fmul_rn(m, 0.25f));
     }
 
     __device__ static uint2 phase1(const uint8_t* tile, int ctid, const QuantParams& p)
