@@ -280,17 +280,17 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 // max over |bf16| of a packed pair, NaN-propagating, as a bf16x2 word.
 __device__ __forceinline__ uint32_t habs_max2(uint32_t acc, uint32_t w)
 {
-    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&acc);
-    uint32_t wa = w & 0x7FFF7FFFu;
-    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&wa);
-    __nv_bfloat162 m = __hmax2_nan(a, b);
-    return *reinterpret_cast<uint32_t*>(&m);
+    // one max.NaN.xorsign.abs per pair: magnitude max(|acc|, |w|), NaN kept;
+    // the sign bits it leaves are meaningless and hmax_to_float drops them
+    uint32_t m;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(acc), "r"(w));
+    return m;
 }
 
 // Larger half of a bf16x2 |.| accumulator as a float (NaN-propagating).
 __device__ __forceinline__ float hmax_to_float(uint32_t acc)
 {
-    const uint32_t lo = acc & 0xFFFFu, hi = acc >> 16;
+    const uint32_t lo = acc & 0x7FFFu, hi = (acc >> 16) & 0x7FFFu;
     // non-negative bf16 bit patterns order like their values; NaN > Inf > finite
     return __uint_as_float((lo > hi ? lo : hi) << 16);
 }
@@ -316,6 +316,23 @@ __device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi)
 {
     uint32_t r;
     asm("{\n.reg .b8 t;\ncvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\ncvt.u32.u8 %0, t;\n}" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight floats to four bytes of E2M1 codes, nearest-even, saturating: v0 in
+// the low nibble of byte 0, v1 in its high nibble, and so on.
+__device__ __forceinline__ uint32_t e2m1x8_rn(float v0, float v1, float v2, float v3, float v4, float v5, float v6,
+                                              float v7)
+{
+    uint32_t r;
+    asm("{\n.reg .b8 b0, b1, b2, b3;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        "mov.b32 %0, {b0, b1, b2, b3};\n}"
+        : "=r"(r)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
     return r;
 }
 

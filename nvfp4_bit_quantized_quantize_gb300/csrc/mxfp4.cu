@@ -95,14 +95,11 @@ __global__ void __launch_bounds__(kMxThreads) mxfp4_quantize_kernel(const MxArgs
                 uint32_t packed[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    uint32_t word = 0;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t x2 = w[4 * i + j];
-                        const uint32_t byte = e2m1x2_rn(__fmul_rn(bf16lo(x2), inv), __fmul_rn(bf16hi(x2), inv));
-                        word |= byte << (8 * j);
-                    }
-                    packed[i] = word;
+                    const uint32_t* x = &w[4 * i];
+                    packed[i] = e2m1x8_rn(__fmul_rn(bf16lo(x[0]), inv), __fmul_rn(bf16hi(x[0]), inv),
+                                          __fmul_rn(bf16lo(x[1]), inv), __fmul_rn(bf16hi(x[1]), inv),
+                                          __fmul_rn(bf16lo(x[2]), inv), __fmul_rn(bf16hi(x[2]), inv),
+                                          __fmul_rn(bf16lo(x[3]), inv), __fmul_rn(bf16hi(x[3]), inv));
                 }
                 c0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }

@@ -117,12 +117,8 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], float ba
         for (int j = 0; j < 16; ++j)
             v[j] = sr_grid_value(v[j], sr_threshold(ws[j >> 2], (uint32_t)(j & 3)));
     }
-    uint32_t bytes[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        bytes[j] = e2m1x2_rn(v[2 * j], v[2 * j + 1]);
-    lo32 = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
-    hi32 = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+    lo32 = e2m1x8_rn(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+    hi32 = e2m1x8_rn(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
     return sb;
 }
 
