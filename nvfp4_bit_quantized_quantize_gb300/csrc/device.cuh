@@ -200,6 +200,50 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// ---- warp-converged issue: the whole warp runs the issuing loop (so the
+// descriptors and addresses stay warp-uniform) and only the lane with
+// `issue` != 0 executes the tcgen05 instruction, under a predicate.
+__device__ __forceinline__ void mma_nvf4_by(uint32_t issue, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.b32 p, %6, 0;\nsetp.ne.b32 q, %7, 0;\n"
+        "@q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.block16 [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(issue)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf4_by(uint32_t issue, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.b32 p, %6, 0;\nsetp.ne.b32 q, %7, 0;\n"
+        "@q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.block32 [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(issue)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_cp_32x128b_x4_by(uint32_t issue, uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("{\n.reg .pred q;\nsetp.ne.b32 q, %2, 0;\n@q tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n}\n" ::"r"(
+                     taddr),
+                 "l"(sdesc), "r"(issue)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_by(uint32_t issue, uint64_t* bar)
+{
+    asm volatile(
+        "{\n.reg .pred q;\nsetp.ne.b32 q, %1, 0;\n"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar)),
+        "r"(issue)
+        : "memory");
+}
+
 // Copy a 32-row x 16-byte block of shared memory into tmem, replicated into
 // the four 32-lane quarters (4 columns per lane).
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
