@@ -79,7 +79,7 @@ bool encode_sf_atom_map(CUtensorMap* map, const uint8_t* sf, int64_t rows, int64
 
 // ----------------------------------------------------------------- probe ----
 namespace {
-__global__ void encode_probe_kernel(const float* v, const uint8_t* r, int64_t n, uint8_t* e4m3, uint8_t* rn,
+__global__ void encode_probe_kernel(const float* v, const uint16_t* r, int64_t n, uint8_t* e4m3, uint8_t* rn,
                                     uint8_t* sr)
 {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -94,7 +94,7 @@ __global__ void encode_probe_kernel(const float* v, const uint8_t* r, int64_t n,
 }
 }  // namespace
 
-nvfp4_status launch_encode_probe(const float* v, const uint8_t* r, int64_t n, uint8_t* e4m3, uint8_t* rn,
+nvfp4_status launch_encode_probe(const float* v, const uint16_t* r, int64_t n, uint8_t* e4m3, uint8_t* rn,
                                  uint8_t* sr, cudaStream_t stream)
 {
     if (n == 0)
@@ -386,7 +386,7 @@ const char* nvfp4_status_str(nvfp4_status s)
     return "unknown status";
 }
 
-nvfp4_status nvfp4_encode_probe(const float* v, const uint8_t* r, int64_t n, uint8_t* e4m3_out,
+nvfp4_status nvfp4_encode_probe(const float* v, const uint16_t* r, int64_t n, uint8_t* e4m3_out,
                                 uint8_t* e2m1_rn_out, uint8_t* e2m1_sr_out, nvfp4_stream_t stream)
 {
     if (!v || n < 0)

@@ -62,7 +62,7 @@ nvfp4_status launch_mxfp4_quantize(const void* x, int64_t rows, int64_t cols, in
 nvfp4_status launch_quant_noise(const void* x, int64_t rows, int64_t cols, int64_t ld, const uint8_t* q,
                                 const uint8_t* sf, const float* g_dec, double* sums, cudaStream_t stream);
 
-nvfp4_status launch_encode_probe(const float* v, const uint8_t* r, int64_t n, uint8_t* e4m3, uint8_t* rn,
+nvfp4_status launch_encode_probe(const float* v, const uint16_t* r, int64_t n, uint8_t* e4m3, uint8_t* rn,
                                  uint8_t* sr, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link

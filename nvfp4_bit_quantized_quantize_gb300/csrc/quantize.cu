@@ -110,12 +110,12 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], float ba
             v[j] = __fmul_rn(x[j], f);
     }
     if (mode == NVFP4_ROUND_SR) {
+        // elements 4m..4m+3 round with Philox word m
         const U4 w = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, (uint32_t)seed,
                                    (uint32_t)(seed >> 32));
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            v[j] = sr_grid_value(v[j], sr_threshold(ws[j >> 2], (uint32_t)(j & 3)));
+        lo32 = e2m1x4_sr(v[0], v[1], v[2], v[3], w.x) | (e2m1x4_sr(v[4], v[5], v[6], v[7], w.y) << 16);
+        hi32 = e2m1x4_sr(v[8], v[9], v[10], v[11], w.z) | (e2m1x4_sr(v[12], v[13], v[14], v[15], w.w) << 16);
+        return sb;
     }
     lo32 = e2m1x8_rn(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
     hi32 = e2m1x8_rn(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);

@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
         L.or_mx_gemm_f64_sampled.restype = None
         L.or_e2m1_rn_many.argtypes = [p, i64, p]
         L.or_e2m1_sr_many.argtypes = [p, p, i64, p]
+        L.or_sr_values.argtypes = [u64, u64, p]
+        L.or_sr_values.restype = None
         L.or_e4m3_rn_sat_many.argtypes = [p, i64, p]
         _lib = L
     return _lib
@@ -128,8 +130,9 @@ def e2m1_rn(v: float) -> int:
     return lib().or_e2m1_rn(float(v))
 
 
-def e2m1_sr(v: float, r: int) -> int:
-    return lib().or_e2m1_sr(float(v), int(r))
+def e2m1_sr(v: float, R: int) -> int:
+    """Stochastic rounding of v with the 16-bit random value R."""
+    return lib().or_e2m1_sr(float(v), int(R))
 
 
 def e4m3_value(code: int) -> float:
@@ -147,9 +150,9 @@ def e2m1_rn_many(v: np.ndarray) -> np.ndarray:
     return out
 
 
-def e2m1_sr_many(v: np.ndarray, r: np.ndarray) -> np.ndarray:
+def e2m1_sr_many(v: np.ndarray, R: np.ndarray) -> np.ndarray:
     v = _c(v, np.float32)
-    r = _c(r, np.uint8)
+    r = _c(R, np.uint16)
     out = np.empty(v.size, np.uint8)
     lib().or_e2m1_sr_many(_ptr(v), _ptr(r), v.size, _ptr(out))
     return out
@@ -167,6 +170,13 @@ def philox4x32_10(ctr, key) -> np.ndarray:
     k = _c(key, np.uint32)
     out = np.empty(4, np.uint32)
     lib().or_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def sr_values(seed: int, blk: int) -> np.ndarray:
+    """The 16-bit random values of the 16 elements of output block blk."""
+    out = np.empty(16, np.uint32)
+    lib().or_sr_values(seed, blk, _ptr(out))
     return out
 
 

@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 
 def _probe(v, r=None):
     vt = torch.from_numpy(np.ascontiguousarray(v, np.float32)).cuda()
-    rt = torch.from_numpy(np.ascontiguousarray(r, np.uint8)).cuda() if r is not None else None
+    rt = torch.from_numpy(np.ascontiguousarray(r, np.uint16).view(np.int16)).cuda() if r is not None else None
     n = v.size
     e4 = torch.empty(n, dtype=torch.uint8, device="cuda")
     rn = torch.empty(n, dtype=torch.uint8, device="cuda")
@@ -58,10 +58,17 @@ def test_e2m1_rn_encoder_matches_oracle():
 
 
 def test_e2m1_sr_encoder_matches_oracle():
+    # every 16-bit random value on grid points, ties, near-threshold and random
+    # inputs; then random (value, random value) pairs
     rng = np.random.default_rng(3)
-    vals = np.concatenate([rng.uniform(-7, 7, 2000), [0.25, 0.75, 1.0 + 1 / 512, 2.0, 5.9999, 6.0, -0.0, 0.0,
-                                                     0.001, 3.5, 4.0 + 1 / 64, 1e9, -np.inf]]).astype(np.float32)
-    v = np.repeat(vals, 256)
-    r = np.tile(np.arange(256, dtype=np.uint8), vals.size)
+    vals = np.concatenate([rng.uniform(-7, 7, 40), [0.25, 0.75, 1.0 + 1 / 512, 2.0, 5.9999, 6.0, -0.0, 0.0,
+                                                   0.001, 3.5, 4.0 + 1 / 64, 1e9, -np.inf, 1.0 + 2 ** -17,
+                                                   0.5 - 2 ** -25]]).astype(np.float32)
+    v = np.repeat(vals, 65536)
+    r = np.tile(np.arange(65536, dtype=np.uint16), vals.size)
     _, _, sr = _probe(v, r)
     assert np.array_equal(sr, O.e2m1_sr_many(v, r))
+    v2 = rng.uniform(-6.5, 6.5, 2_000_000).astype(np.float32)
+    r2 = rng.integers(0, 65536, v2.size).astype(np.uint16)
+    _, _, sr2 = _probe(v2, r2)
+    assert np.array_equal(sr2, O.e2m1_sr_many(v2, r2))

@@ -79,38 +79,79 @@ def test_e2m1_rn_monotone():
 # ------------------------------------------------------------ E2M1 SR ----
 
 def _closed_form_sr_mean(a):
-    """E[SR(a)] = lo + gap * round_half_down(t) / 256 with t = 256 (a-lo)/gap."""
+    """E[SR(a)] = lo + gap * floor(2^16 f) / 2^16 with f = (a - lo) / gap: the
+    up-probability is the fraction kept to 16 bits."""
     grid = PAGE_E2M1_MAGNITUDES
     if a >= 6:
         return 6.0
     lo = max(g for g in grid if g <= a)
     hi = grid[grid.index(lo) + 1]
-    t = (a - lo) / (hi - lo) * 256
-    k = math.ceil(t - 0.5)  # number of bytes r with r + 0.5 < t
-    return lo + (hi - lo) * k / 256
+    f16 = math.floor((a - lo) / (hi - lo) * 65536)
+    return lo + (hi - lo) * f16 / 65536
 
 
-def test_e2m1_sr_exact_distribution_over_all_bytes():
-    # Over the 256 random bytes the up-probability is exact: the mean equals
-    # the closed form, and on the grid nothing moves.
+ALL_R = np.arange(65536, dtype=np.uint16)
+
+
+def test_e2m1_sr_exact_distribution_over_all_random_values():
+    # Over all 2^16 random values the up-probability is exact: the mean equals
+    # the closed form, only the two neighbours occur, and on the grid nothing
+    # moves.
     rng = np.random.default_rng(3)
-    for a in list(rng.uniform(0, 6.5, 300)) + PAGE_E2M1_MAGNITUDES + [0.25, 0.75, 1.0 + 1 / 512]:
+    for a in list(rng.uniform(0, 6.5, 200)) + PAGE_E2M1_MAGNITUDES + [0.25, 0.75, 1.0 + 1 / 512, 5.999]:
         a = float(np.float32(a))
-        codes = O.e2m1_sr_many(np.full(256, a, np.float32), np.arange(256, dtype=np.uint8))
-        mean = np.mean([O.e2m1_value(c) for c in codes])
+        codes = O.e2m1_sr_many(np.full(65536, a, np.float32), ALL_R)
+        vals = np.array([O.e2m1_value(c) for c in np.unique(codes)])
+        counts = np.array([np.sum(codes == c) for c in np.unique(codes)])
+        mean = float(np.sum(vals * counts) / 65536)
         assert mean == pytest.approx(_closed_form_sr_mean(a), abs=1e-12), a
-        # only the two neighbours occur
-        assert len(set(codes.tolist())) <= 2
+        assert len(vals) <= 2
     for m in PAGE_E2M1_MAGNITUDES:
-        codes = O.e2m1_sr_many(np.full(256, m, np.float32), np.arange(256, dtype=np.uint8))
-        assert set(O.e2m1_value(c) for c in codes) == {m}
+        codes = O.e2m1_sr_many(np.full(65536, m, np.float32), ALL_R)
+        assert set(O.e2m1_value(c) for c in np.unique(codes)) == {m}
 
 
-def test_e2m1_sr_unbiased_where_t_is_integer():
-    # t integer -> exactly unbiased: E[q] == a
-    for a in [0.25, 0.125, 1.25, 1.0 + 3 / 512, 2.5, 3.0 + 17 / 256, 5.0, 4.0 + 2 * 100 / 256]:
-        codes = O.e2m1_sr_many(np.full(256, a, np.float32), np.arange(256, dtype=np.uint8))
-        assert np.mean([O.e2m1_value(c) for c in codes]) == pytest.approx(a, abs=1e-12)
+def test_e2m1_sr_unbiased_where_the_fraction_has_16_bits():
+    # f exact in 16 bits -> exactly unbiased: E[q] == a; and the bias never
+    # exceeds one 2^-16 step of the gap
+    for a in [0.25, 0.125, 1.25, 1.0 + 3 / 512, 2.5, 3.0 + 17 / 256, 5.0, 4.0 + 2 * 100 / 256, 1.0 + 2 ** -17]:
+        codes = O.e2m1_sr_many(np.full(65536, a, np.float32), ALL_R)
+        mean = float(np.mean([O.e2m1_value(c) for c in codes]))
+        gap = 0.5 if a < 2 else (1.0 if a < 4 else 2.0)
+        assert a - gap * 2 ** -16 <= mean <= a + 1e-12
+        if (a * 65536 / gap) % 1 == 0:
+            assert mean == pytest.approx(a, abs=1e-12)
+
+
+def test_e2m1_sr_carry_rule_hand_cases():
+    # 1.25 lies half way from 1 to 1.5: up exactly for R >= 2^15
+    assert O.e2m1_sr(1.25, 0x7FFF) == 0x2 and O.e2m1_sr(1.25, 0x8000) == 0x3
+    # 5 lies half way from 4 to 6
+    assert O.e2m1_sr(5.0, 0x7FFF) == 0x6 and O.e2m1_sr(5.0, 0x8000) == 0x7
+    # below 0.5 the grid step is 0.5 (from 0): 0.125 is a quarter of the way
+    assert O.e2m1_sr(0.125, 0xBFFF) == 0x0 and O.e2m1_sr(0.125, 0xC000) == 0x1
+    # signs are kept, also on the way to zero; 6 and beyond saturate
+    assert O.e2m1_sr(-0.125, 0x0000) == 0x8 and O.e2m1_sr(-0.125, 0xFFFF) == 0x9
+    assert O.e2m1_sr(7.5, 0xFFFF) == 0x7 and O.e2m1_sr(-100.0, 0) == 0xF
+
+
+def test_sr_values_are_uniform_16_bit_and_use_each_word_twice():
+    # every element draws 16 bits; over many blocks each element's values are
+    # uniform (chi-square on 256 bins of the high byte) and the four values of
+    # one word use its 32 bits exactly twice (bit counts add up)
+    n = 4096
+    vals = np.array([O.sr_values(11, b) for b in range(n)], np.int64)
+    assert vals.max() < 65536
+    for j in range(16):
+        hist = np.bincount(vals[:, j] >> 8, minlength=256)
+        chi2 = float(np.sum((hist - n / 256) ** 2 / (n / 256)))
+        assert chi2 < 400, (j, chi2)
+    pop = lambda x: bin(int(x)).count("1")
+    for b in range(64):
+        v = vals[b]
+        w = O.philox4x32_10([b, 0, 0, 0], [11, 0])
+        for m in range(4):
+            assert sum(pop(v[4 * m + i]) for i in range(4)) == 2 * pop(w[m])
 
 
 def test_sr_unbiased_over_seeds_through_quantize():
