@@ -165,56 +165,44 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 constexpr uint32_t kSwizzleNone = 0;
 constexpr uint32_t kSwizzle128B = 2;
 
-// ---- tcgen05 issue, warp-converged: the whole warp runs the issuing loop
-// (so descriptors and addresses stay warp-uniform) and only the lane with
-// `issue` != 0 executes the instruction, under a predicate.
-//   mma_nvf4_by  D(tmem) (+)= A(smem) B(smem)^T, E2M1 operands, E4M3
-//                block-16 scales read from tmem (NVFP4)
-//   mma_mxf4_by  the same with UE8M0 block-32 scales (MXFP4): two scales per
-//                row per K = 64 step, bytes 0 and 1 of the row's scale column
-//   tmem_cp_32x128b_x4_by  a 32-row x 16-byte block of shared memory into
-//                tmem, replicated into the four 32-lane quarters
-//   tc_commit_by arrive once on `bar` when all earlier tcgen05 work of the
-//                issuing lane has completed
-__device__ __forceinline__ void mma_nvf4_by(uint32_t issue, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                            uint32_t accumulate)
+// D(tmem) (+)= A(smem) x B(smem)^T with E2M1 operands and E4M3 block-16 scales
+// read from tmem.
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
     asm volatile(
-        "{\n.reg .pred p, q;\nsetp.ne.b32 p, %6, 0;\nsetp.ne.b32 q, %7, 0;\n"
-        "@q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.block16 [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.block16 [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
             d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(issue)
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
 
-__device__ __forceinline__ void mma_mxf4_by(uint32_t issue, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                            uint32_t accumulate)
+// The same with UE8M0 block-32 scales (MXFP4): two scales per row per K = 64
+// step, bytes 0 and 1 of the row's 32-bit scale column (scale-factor id 0).
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
     asm volatile(
-        "{\n.reg .pred p, q;\nsetp.ne.b32 p, %6, 0;\nsetp.ne.b32 q, %7, 0;\n"
-        "@q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.block32 [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.block32 [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
             d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(issue)
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_cp_32x128b_x4_by(uint32_t issue, uint32_t taddr, uint64_t sdesc)
+// Copy a 32-row x 16-byte block of shared memory into tmem, replicated into
+// the four 32-lane quarters (4 columns per lane).
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
 {
-    asm volatile("{\n.reg .pred q;\nsetp.ne.b32 q, %2, 0;\n@q tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n}\n" ::"r"(
-                     taddr),
-                 "l"(sdesc), "r"(issue)
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
                  : "memory");
-}
-
-__device__ __forceinline__ void tc_commit_by(uint32_t issue, uint64_t* bar)
-{
-    asm volatile(
-        "{\n.reg .pred q;\nsetp.ne.b32 q, %1, 0;\n"
-        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar)),
-        "r"(issue)
-        : "memory");
 }
 
 // 32 lanes x 32 columns of 32-bit accumulator: thread i gets lane base+i.

@@ -66,13 +66,13 @@ constexpr uint32_t kIdescNvf4 = mma_idesc<false>(BM, BN);
 constexpr uint32_t kIdescMxf4 = mma_idesc<true>(BM, BN);
 
 template <bool kMx>
-__device__ __forceinline__ void mma_step(uint32_t issue, uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t sfa,
-                                         uint32_t sfb, uint32_t acc)
+__device__ __forceinline__ void mma_step(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t sfa, uint32_t sfb,
+                                         uint32_t acc)
 {
     if constexpr (kMx)
-        mma_mxf4_by(issue, d, adesc, bdesc, kIdescMxf4, sfa, sfb, acc);
+        mma_mxf4(d, adesc, bdesc, kIdescMxf4, sfa, sfb, acc);
     else
-        mma_nvf4_by(issue, d, adesc, bdesc, kIdescNvf4, sfa, sfb, acc);
+        mma_nvf4(d, adesc, bdesc, kIdescNvf4, sfa, sfb, acc);
 }
 
 // kMx = false: NVFP4 (E4M3 block-16 scales, D scaled by ga * gb);
@@ -154,11 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&ctl->full[s], phase, ws, nullptr);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------ MMA issuer ----
-        // The whole warp runs this loop, so every descriptor and address is
-        // warp-uniform; lane 0 alone executes each tcgen05 instruction.
-        const uint32_t issue = lane == 0 ? 1u : 0u;
         const uint32_t base = smem_u32(smem);
         const uint64_t a_desc = smem_desc(base, 16, 1024, kSwizzle128B);
         const uint64_t b_desc = smem_desc(base + kABytes, 16, 1024, kSwizzle128B);
@@ -181,13 +178,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k_left >= BK) {
 #pragma unroll
                     for (uint32_t j = 0; j < 4; ++j) {
-                        tmem_cp_32x128b_x4_by(issue, sfa_t + 4 * j, sfa_desc + off + 32 * j);
-                        tmem_cp_32x128b_x4_by(issue, sfb_t + 8 * j, sfb_desc + off + 32 * j);
-                        tmem_cp_32x128b_x4_by(issue, sfb_t + 8 * j + 4, sfb_desc + off + 128 + 32 * j);
+                        tmem_cp_32x128b_x4(sfa_t + 4 * j, sfa_desc + off + 32 * j);
+                        tmem_cp_32x128b_x4(sfb_t + 8 * j, sfb_desc + off + 32 * j);
+                        tmem_cp_32x128b_x4(sfb_t + 8 * j + 4, sfb_desc + off + 128 + 32 * j);
                     }
 #pragma unroll
                     for (uint32_t j = 0; j < 4; ++j)
-                        mma_step<kMx>(issue, tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
+                        mma_step<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
                                       sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
                 } else {
                     // last stage: K = 64 steps, the final one possibly half
@@ -195,25 +192,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // zero padding of the last atom)
                     const uint32_t kk = (k_left + 63) / 64;
                     for (uint32_t j = 0; j < kk; ++j) {
-                        tmem_cp_32x128b_x4_by(issue, sfa_t + 4 * j, sfa_desc + off + 32 * j);
-                        tmem_cp_32x128b_x4_by(issue, sfb_t + 8 * j, sfb_desc + off + 32 * j);
-                        tmem_cp_32x128b_x4_by(issue, sfb_t + 8 * j + 4, sfb_desc + off + 128 + 32 * j);
+                        tmem_cp_32x128b_x4(sfa_t + 4 * j, sfa_desc + off + 32 * j);
+                        tmem_cp_32x128b_x4(sfb_t + 8 * j, sfb_desc + off + 32 * j);
+                        tmem_cp_32x128b_x4(sfb_t + 8 * j + 4, sfb_desc + off + 128 + 32 * j);
                     }
                     for (uint32_t j = 0; j < kk; ++j)
-                        mma_step<kMx>(issue, tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
+                        mma_step<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
                                       sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
                 }
-                tc_commit_by(issue, &ctl->empty[s]);
+                tc_commit(&ctl->empty[s]);
                 if (++s == kStages) {
                     s = 0;
                     phase ^= 1;
                 }
             }
-            tc_commit_by(issue, &ctl->tmem_full);
+            tc_commit(&ctl->tmem_full);
         }
     mma_done:
-        // all tensor-core work issued by lane 0 completes before teardown
-        tc_commit_by(issue, &ctl->drain);
+        // all tensor-core work issued by this thread completes before teardown
+        tc_commit(&ctl->drain);
         mbar_wait(&ctl->drain, 0, ws, nullptr);
     } else if (warp >= 2) {
         // -------------------------------------------------------- epilogue ----
