@@ -78,7 +78,8 @@ def source_hash(files):
     return h.hexdigest()[:16]
 
 
-GEMM_SOURCES = ["nvfp4_bit_quantized_quantize_gb300/csrc/gemm.cu", "nvfp4_bit_quantized_quantize_gb300/csrc/device.cuh"]
+GEMM_SOURCES = ["nvfp4_bit_quantized_quantize_gb300/csrc/gemm.cu", "nvfp4_bit_quantized_quantize_gb300/csrc/gemm_common.cuh",
+                "nvfp4_bit_quantized_quantize_gb300/csrc/device.cuh"]
 
 
 def traffic_for(kernel: str, src_hash: str):

@@ -203,3 +203,47 @@ def test_quantize_dual_full_size_activation():
     _assert_same(sf, rsf, "row scales")
     _assert_same(qT, rqT, "transformed codes")
     _assert_same(sfT, rsfT, "transformed scales")
+
+
+# ------------------------------------------- degenerate inputs, every form ----
+
+def test_rht_dual_2d_on_zero_and_tiny_tensors():
+    """amax = 0 gives g = 0, zero scales and sign-only codes in every form; a
+    subnormal-range tensor saturates s_enc like the oracle does."""
+    z = synth.f32_to_bf16_bits(np.array([[0.0, -0.0] * 24] * 32, np.float32))  # 32 x 48
+    qT, sfT, g, st = rht_quantize(z, 3, nv.SR, 1)
+    rqT, rsfT, rg = O.rht_quantize(z, 3, O.SR, 1)
+    assert st == 0 and g == 0.0 == rg
+    _assert_same(qT, rqT, "rht codes")
+    _assert_same(sfT, rsfT, "rht scales")
+    q, sf, g, qT, sfT, gT, st = quantize_dual(z, nv.SR, 2, 3, nv.SR, 4)
+    assert st == 0 and g == 0.0 and gT == 0.0
+    _assert_same(q, O.quantize(z, O.SR, 2)[0], "dual row codes")
+    _assert_same(qT, O.rht_quantize(z, 3, O.SR, 4)[0], "dual rht codes")
+    q, sf, qT, sfT, g, st = quantize_2d(z)
+    assert st == 0 and g == 0.0 and not sf.any() and not sfT.any()
+    tiny = np.zeros((32, 48), np.float32)
+    tiny[3, 5], tiny[17, 40], tiny[30, 0] = 2.0 ** -130, -2.0 ** -126, 2.0 ** -133
+    tb = synth.f32_to_bf16_bits(tiny)
+    q, sf, g, qT, sfT, gT, st = quantize_dual(tb, nv.RN, 0, 5, nv.SR, 6)
+    rq, rsf, rg = O.quantize(tb, O.RN, 0)
+    rqT, rsfT, rgT = O.rht_quantize(tb, 5, O.SR, 6)
+    assert st == 0 and g == rg and gT == rgT
+    _assert_same(q, rq, "tiny row codes")
+    _assert_same(qT, rqT, "tiny rht codes")
+    _assert_same(sfT, rsfT, "tiny rht scales")
+
+
+def test_nonfinite_input_is_reported_by_every_form():
+    x = synth.normal_bf16((64, 128), 4, 0)
+    x[9, 70] = 0x7F80  # +inf
+    assert rht_quantize(x, 1, nv.SR, 2)[3] == 4
+    assert quantize_dual(x, nv.RN, 0, 1, nv.SR, 2)[6] == 4
+    assert quantize_2d(x)[5] == 4
+    # finite input whose Hadamard sums overflow binary32: the transformed amax
+    # is not finite, which the Hadamard forms report
+    big = np.full((16, 16), 3.0e38, np.float32)
+    bb = synth.f32_to_bf16_bits(big)
+    assert rht_quantize(bb, 0, nv.RN, 0)[3] == 4
+    with pytest.raises(O.OracleError):
+        O.rht_quantize(bb, 0, O.RN, 0)
