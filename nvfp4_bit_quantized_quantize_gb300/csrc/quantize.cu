@@ -105,9 +105,11 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], float ba
         for (int j = 0; j < 16; ++j)
             v[j] = (x[j] == 0.0f) ? x[j] : __fmul_rn(x[j], f);
     } else {
+        // elements j and j + 8 share one packed multiply
+        const uint64_t ff = f2_pack(f, f);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            v[j] = __fmul_rn(x[j], f);
+        for (int j = 0; j < 8; ++j)
+            f2_unpack(f2_mul(f2_pack(x[j], x[j + 8]), ff), v[j], v[j + 8]);
     }
     if (mode == NVFP4_ROUND_SR) {
         // elements 4m..4m+3 round with Philox word m
@@ -312,49 +314,71 @@ struct OpRht {
         tma_load_2d(dst + 8192, m, bar, (int32_t)(ct * 128 + 64), (int32_t)(tt * 64));
     }
 
-    // y = (1/4) H16 D v for this thread's channel and token block (without
-    // the exact final 1/4 when kQuarter is false).
-    template <bool kQuarter = true>
-    __device__ static void transform(const uint8_t* tile, int ctid, uint32_t signs, float (&y)[16])
+    // D v for this thread's channel and token block, as pairs P[k] =
+    // (element k, element k + 8), and the butterflies of strides 1, 2 and 4:
+    // with that pairing every butterfly of those strides joins lane with
+    // lane, so one packed add and one packed subtract do two of them.
+    __device__ static void butterflies_124(const uint8_t* tile, int ctid, uint32_t signs, uint64_t (&P)[8])
     {
         const int lane = ctid & 31, cw = ctid >> 5;
         const uint32_t tb = cw >> 2, cl = (cw & 3) * 32 + lane;
         const uint8_t* half = tile + (cl >> 6) * 8192;
         const uint32_t cb = cl & 63;
+        float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint32_t row = tb * 16 + i;
             const uint32_t h = *reinterpret_cast<const uint16_t*>(half + sw128(row, cb >> 3) + (cb & 7) * 2);
-            y[i] = __uint_as_float((h << 16) ^ ((signs << (31 - i)) & 0x80000000u));
+            v[i] = __uint_as_float((h << 16) ^ ((signs << (31 - i)) & 0x80000000u));
         }
 #pragma unroll
-        for (int hs = 1; hs < 16; hs <<= 1) {
+        for (int k = 0; k < 8; ++k)
+            P[k] = f2_pack(v[k], v[k + 8]);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                if (i & hs)
+        for (int hs = 1; hs < 8; hs <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (k & hs)
                     continue;
-                const float a = y[i], b = y[i + hs];
-                y[i] = __fadd_rn(a, b);
-                y[i + hs] = __fsub_rn(a, b);
+                const uint64_t a = P[k], b = P[k + hs];
+                P[k] = f2_add(a, b);
+                P[k + hs] = f2_sub(a, b);
             }
         }
-        if constexpr (kQuarter) {
+    }
+
+    // y = (1/4) H16 D v for this thread's channel and token block: the
+    // butterflies in stride order 1, 2, 4, 8, then the exact 1/4.
+    __device__ static void transform(const uint8_t* tile, int ctid, uint32_t signs, float (&y)[16])
+    {
+        uint64_t P[8];
+        butterflies_124(tile, ctid, signs, P);
+        const uint64_t quarter = f2_pack(0.25f, 0.25f);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                y[i] = __fmul_rn(y[i], 0.25f);
+        for (int k = 0; k < 8; ++k) {
+            float a, b;
+            f2_unpack(P[k], a, b);
+            f2_unpack(f2_mul(f2_pack(__fadd_rn(a, b), __fsub_rn(a, b)), quarter), y[k], y[k + 8]);
         }
     }
 
     // max |y| as float bits (NaN-propagating).  Multiplying by 1/4 is exact
     // and monotone, so max |H16 D v| / 4 equals the max over the scaled values.
+    // The last butterfly maps (a, b) to (a + b, a - b), whose larger
+    // magnitude is rn(|a| + |b|) (rounding is monotone and odd); the two
+    // differ only when a and b are both infinite (NaN against Inf), and both
+    // are non-finite.
     __device__ static uint32_t transformed_amax(const uint8_t* tile, int ctid, const QuantParams& p)
     {
-        float u[16];
-        transform<false>(tile, ctid, p.rht_signs, u);
+        uint64_t P[8];
+        butterflies_124(tile, ctid, p.rht_signs, P);
         float m = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            asm("max.NaN.f32 %0, %1, %2;" : "=f"(m) : "f"(m), "f"(fabsf(u[i])));
+        for (int k = 0; k < 8; ++k) {
+            float a, b;
+            f2_unpack(P[k], a, b);
+            asm("max.NaN.f32 %0, %1, %2;" : "=f"(m) : "f"(m), "f"(__fadd_rn(fabsf(a), fabsf(b))));
+        }
         return __float_as_uint(__fmul_rn(m, 0.25f));
     }
 
