@@ -12,15 +12,22 @@
 // persistent sequence of 128 x 256 output tiles:
 //   warp 0  TMA producer: A/B tiles (128-byte swizzle) and the scale atoms
 //           (3-D tensor boxes of 4 atoms) into a 4-stage shared-memory ring;
-//   warp 1  allocates tensor memory, moves the scale atoms into it
-//           (tcgen05.cp) and issues tcgen05.mma.kind::mxf4nvf4 (K = 64 per
-//           instruction, binary32 accumulator in tensor memory);
+//   warp 1  allocates tensor memory and issues tcgen05.mma.kind::mxf4nvf4
+//           (K = 64 per instruction, binary32 accumulator in tensor memory);
 //   warps 2-9 epilogue, two per tensor-memory lane quarter (128 columns
-//           each): all tcgen05.ld of the accumulator issued before one wait,
-//           the accumulator released, then times ga*gb, round to bf16 (or
-//           keep binary32), and 32-row chunks staged in a 1 KB shared buffer
-//           per warp leave through TMA bulk tensor stores (per-thread row
-//           stores would flood the memory pipe the MMA warp issues through).
+//           each): the accumulator read in two rounds of two tcgen05.ld and
+//           one wait, times ga*gb and rounded to bf16 pairs (binary32 output
+//           is stored round by round), the accumulator released, then
+//           32-row chunks staged in a 1 KB shared buffer per warp leave
+//           through TMA bulk tensor stores (per-thread row stores would flood
+//           the memory pipe the MMA warp issues through);
+//   warps 10-13 one per tensor-memory lane quarter: write each stage's scale
+//           atoms from shared memory into that quarter's lanes with
+//           tcgen05.st (every quarter holds the four 32-row groups of an atom,
+//           the layout the MMA reads), wait for the stores and signal the
+//           MMA warp.  A tcgen05.cp of the atoms would cost the tensor pipe
+//           about 56 cycles per copy, three copies per MMA — half the
+//           kernel's time; stores by these warps take none of it.
 // The MMA warp's issue loop is kept lean: every descriptor is a precomputed
 // base plus a constant offset, the four K = 64 steps of a stage are unrolled.
 // Every wait is bounded; a wait that runs out records NVFP4_ERR_TIMEOUT and
@@ -40,7 +47,9 @@ constexpr int kSfaBytes = (BM / 128) * (BK / 64) * 512;  // 2 KB
 constexpr int kSfbBytes = (BN / 128) * (BK / 64) * 512;  // 4 KB
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
 constexpr int kEpilogueWarps = 8;
-constexpr int kThreads = (2 + kEpilogueWarps) * 32;
+constexpr int kScaleWarps = 4;
+constexpr int kFirstScaleWarp = 2 + kEpilogueWarps;
+constexpr int kThreads = (2 + kEpilogueWarps + kScaleWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = BN;             // fp32 accumulator: 128 lanes x 256 columns
 constexpr uint32_t kSfColsPerStage = 16 + 32; // SFA 4 steps x 4 cols, SFB 4 steps x 8 cols
@@ -53,6 +62,7 @@ static_assert(kAccCols + kStages * kSfSlotStride <= kTmemCols, "tensor memory bu
 struct GemmCtl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t sf_ready[kStages];  // scale atoms of the stage are in tensor memory
     uint64_t tmem_full;
     uint64_t tmem_empty;
     uint64_t drain;
@@ -100,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl->full[s], 1);
             mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->sf_ready[s], kScaleWarps);
         }
         mbar_init(&ctl->tmem_full, 1);
         mbar_init(&ctl->tmem_empty, kEpilogueWarps);
@@ -159,8 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t base = smem_u32(smem);
         const uint64_t a_desc = smem_desc(base, 16, 1024, kSwizzle128B);
         const uint64_t b_desc = smem_desc(base + kABytes, 16, 1024, kSwizzle128B);
-        const uint64_t sfa_desc = smem_desc(base + kABytes + kBBytes, 0, 128, kSwizzleNone);
-        const uint64_t sfb_desc = smem_desc(base + kABytes + kBBytes + kSfaBytes, 0, 128, kSwizzleNone);
         constexpr uint32_t kStageDesc = kStageBytes >> 4;  // stage stride in descriptor units
         uint32_t s = 0, phase = 0, titer = 0;
         for (uint32_t t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++titer) {
@@ -168,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after();
             for (uint32_t ks = 0; ks < kstages; ++ks) {
-                if (!mbar_wait(&ctl->full[s], phase, ws, abort))
+                // the scale warps saw the stage's loads complete before they signalled
+                if (!mbar_wait(&ctl->sf_ready[s], phase, ws, abort))
                     goto mma_done;
                 tc_fence_after();
                 const uint64_t off = (uint64_t)(s * kStageDesc);
@@ -176,12 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sfb_t = sfa_t + 16;
                 const uint32_t k_left = (uint32_t)args.K - ks * BK;
                 if (k_left >= BK) {
-#pragma unroll
-                    for (uint32_t j = 0; j < 4; ++j) {
-                        tmem_cp_32x128b_x4(sfa_t + 4 * j, sfa_desc + off + 32 * j);
-                        tmem_cp_32x128b_x4(sfb_t + 8 * j, sfb_desc + off + 32 * j);
-                        tmem_cp_32x128b_x4(sfb_t + 8 * j + 4, sfb_desc + off + 128 + 32 * j);
-                    }
 #pragma unroll
                     for (uint32_t j = 0; j < 4; ++j)
                         mma_step<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
@@ -191,11 +195,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // filled (codes past K read as zeros, their scales are the
                     // zero padding of the last atom)
                     const uint32_t kk = (k_left + 63) / 64;
-                    for (uint32_t j = 0; j < kk; ++j) {
-                        tmem_cp_32x128b_x4(sfa_t + 4 * j, sfa_desc + off + 32 * j);
-                        tmem_cp_32x128b_x4(sfb_t + 8 * j, sfb_desc + off + 32 * j);
-                        tmem_cp_32x128b_x4(sfb_t + 8 * j + 4, sfb_desc + off + 128 + 32 * j);
-                    }
                     for (uint32_t j = 0; j < kk; ++j)
                         mma_step<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
                                       sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
@@ -212,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // all tensor-core work issued by this thread completes before teardown
         tc_commit(&ctl->drain);
         mbar_wait(&ctl->drain, 0, ws, nullptr);
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < kFirstScaleWarp) {
         // -------------------------------------------------------- epilogue ----
         const uint32_t q = warp & 3;             // tensor-memory lane quarter of this warp
         const uint32_t half = (warp - 2) >> 2;   // columns 128*half .. +127
@@ -224,26 +223,90 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after();
             const int32_t c0 = (int32_t)(tn * BN + half * 128);
+            const int32_t row0 = (int32_t)(tm * BM + q * 32);
+            const bool live = c0 < args.N && row0 < args.M;
+            uint8_t* buf = store_buf + (warp - 2) * kStoreBufBytes;
             const uint32_t taddr = tmem + ((q * 32) << 16) + half * 128;
-            uint32_t r[4][32];
+            uint32_t p[64];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
-            tmem_ld_wait();
+            for (int h = 0; h < 4; ++h) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + h * 32, r);
+                tmem_ld_wait();
+                if (args.out_f32) {
+                    if (live)
+                        epilogue_store_f32(r, alpha, row0, c0 + h * 32, args, buf, &tma_d, lane);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        p[h * 16 + e] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * e]), alpha),
+                                                    __fmul_rn(__uint_as_float(r[2 * e + 1]), alpha));
+                }
+            }
             // the accumulator is free once every load has landed in registers
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&ctl->tmem_empty);
-            if (c0 >= args.N)
-                continue;
-            const int32_t row0 = (int32_t)(tm * BM + q * 32);
-            if (row0 >= args.M)
-                continue;
-            epilogue_store(r, alpha, row0, c0, args, store_buf + (warp - 2) * kStoreBufBytes, &tma_d, lane);
+            if (live && !args.out_f32)
+                epilogue_store_bf16(p, row0, c0, args, buf, &tma_d, lane);
         }
         if (lane == 0)
             bulk_wait_all();
+    } else if (warp >= kFirstScaleWarp) {
+        // ----------------------------------------------------- scale warps ----
+        // Stage layout: A's 4 atoms (steps 0..3), then B's row tile 0 steps
+        // 0..3 and row tile 1 steps 0..3, 512 bytes each.  Lane i takes row i
+        // (16 bytes) of every atom: tensor-memory columns slot + 4j .. + 3
+        // for A's step j and slot + 16 + 8j .. + 7 for B's step j (tile 0,
+        // then tile 1), in its quarter's lanes.
+        const uint32_t q = warp & 3;
+        const uint32_t lanes = (q * 32) << 16;
+        uint32_t s = 0, phase = 0;
+        for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            for (uint32_t ks = 0; ks < kstages; ++ks) {
+                int ok = 1;
+                if (lane == 0)
+                    ok = mbar_wait(&ctl->full[s], phase, ws, abort);
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0))
+                    goto scales_done;
+                const uint8_t* sfa_s = smem + (size_t)s * kStageBytes + kABytes + kBBytes + lane * 16;
+                const uint8_t* sfb_s = sfa_s + kSfaBytes;
+                uint32_t v[48];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(sfa_s + j * 512);
+                    const uint4 b0 = *reinterpret_cast<const uint4*>(sfb_s + j * 512);
+                    const uint4 b1 = *reinterpret_cast<const uint4*>(sfb_s + (4 + j) * 512);
+                    v[4 * j] = a.x;
+                    v[4 * j + 1] = a.y;
+                    v[4 * j + 2] = a.z;
+                    v[4 * j + 3] = a.w;
+                    v[16 + 8 * j] = b0.x;
+                    v[16 + 8 * j + 1] = b0.y;
+                    v[16 + 8 * j + 2] = b0.z;
+                    v[16 + 8 * j + 3] = b0.w;
+                    v[16 + 8 * j + 4] = b1.x;
+                    v[16 + 8 * j + 5] = b1.y;
+                    v[16 + 8 * j + 6] = b1.z;
+                    v[16 + 8 * j + 7] = b1.w;
+                }
+                const uint32_t slot = tmem + lanes + kAccCols + s * kSfSlotStride;
+                tmem_st_32x32b_x16(slot, v);
+                tmem_st_32x32b_x16(slot + 16, v + 16);
+                tmem_st_32x32b_x16(slot + 32, v + 32);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ctl->sf_ready[s]);
+                if (++s == kStages) {
+                    s = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+    scales_done:;
     }
 
     __syncthreads();

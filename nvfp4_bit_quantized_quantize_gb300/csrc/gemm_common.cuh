@@ -43,84 +43,83 @@ __device__ __forceinline__ bool edge_chunk(int32_t col, int32_t width, int32_t r
 
 constexpr int kStoreBufBytes = 1024;  // per epilogue warp: 32 rows x 32 bytes
 
-// Store this warp's 32 rows (row0 + lane) x 128 columns (c0 ..) of the
-// accumulator, held in r, times alpha, as bf16 (nearest) or binary32: 32-byte
-// row chunks staged in the warp's 1 KB buffer leave through TMA tensor
-// stores; chunks on the M/N edge take plain stores of the valid elements.
-__device__ __forceinline__ void epilogue_store(const uint32_t (&r)[4][32], float alpha, int32_t row0, int32_t c0,
-                                               const GemmArgs& args, uint8_t* buf, const CUtensorMap* tma_d,
-                                               int lane)
+// Send one 32-row x 32-byte chunk (w: this lane's row) through the warp's
+// staging buffer and a TMA tensor store at (col, row0).
+__device__ __forceinline__ void store_chunk(const uint32_t (&w)[8], int32_t col, int32_t row0, uint8_t* buf,
+                                            const CUtensorMap* tma_d, int lane)
 {
-    if (args.out_f32) {
-        // 16 chunks of 8 columns (32 bytes per row)
+    if (lane == 0)
+        bulk_wait_read0();
+    __syncwarp();
+    reinterpret_cast<uint4*>(buf + lane * 32)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(buf + lane * 32)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tma_d, buf, col, row0);
+        bulk_commit_group();
+    }
+}
+
+// Store this warp's 32 rows (row0 + lane) x 128 columns (c0 ..) held as bf16
+// pairs in p (word j: columns c0 + 2j, c0 + 2j + 1, the first in the low
+// half): 16-column chunks leave through TMA tensor stores; chunks on the M/N
+// edge take plain stores of the valid elements.
+__device__ __forceinline__ void epilogue_store_bf16(const uint32_t (&p)[64], int32_t row0, int32_t c0,
+                                                   const GemmArgs& args, uint8_t* buf, const CUtensorMap* tma_d,
+                                                   int lane)
+{
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-            if (c0 + ch * 8 >= args.N)
-                break;
-            const uint32_t* rr = &r[ch >> 2][(ch & 3) * 8];
-            uint32_t w[8];
+    for (int ch = 0; ch < 8; ++ch) {
+        const int32_t col = c0 + ch * 16;
+        if (col >= args.N)
+            break;
+        uint32_t w[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                w[e] = __float_as_uint(__fmul_rn(__uint_as_float(rr[e]), alpha));
-            if (edge_chunk(c0 + ch * 8, 8, row0, args)) {
-                // ragged edge: plain stores of the elements inside M x N
-                const int32_t row = row0 + lane, col = c0 + ch * 8;
-                if (row < args.M) {
-                    float* dst = static_cast<float*>(args.d) + (int64_t)row * args.ldd + col;
+        for (int e = 0; e < 8; ++e)
+            w[e] = p[ch * 8 + e];
+        if (edge_chunk(col, 16, row0, args)) {
+            const int32_t row = row0 + lane;
+            if (row < args.M) {
+                uint16_t* dst = static_cast<uint16_t*>(args.d) + (int64_t)row * args.ldd + col;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        if (col + e < args.N)
-                            dst[e] = __uint_as_float(w[e]);
-                }
-                continue;
+                for (int e = 0; e < 16; ++e)
+                    if (col + e < args.N)
+                        dst[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
             }
-            if (lane == 0)
-                bulk_wait_read0();
-            __syncwarp();
-            reinterpret_cast<uint4*>(buf + lane * 32)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            reinterpret_cast<uint4*>(buf + lane * 32)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_2d(tma_d, buf, c0 + ch * 8, row0);
-                bulk_commit_group();
-            }
+            continue;
         }
-    } else {
-        // 8 chunks of 16 columns (32 bytes per row)
+        store_chunk(w, col, row0, buf, tma_d, lane);
+    }
+}
+
+// Store 32 rows x 32 columns (c0 ..) of binary32 accumulator values r times
+// alpha, in 8-column chunks, as above.
+__device__ __forceinline__ void epilogue_store_f32(const uint32_t (&r)[32], float alpha, int32_t row0, int32_t c0,
+                                                  const GemmArgs& args, uint8_t* buf, const CUtensorMap* tma_d,
+                                                  int lane)
+{
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            if (c0 + ch * 16 >= args.N)
-                break;
-            const uint32_t* rr = &r[ch >> 1][(ch & 1) * 16];
-            uint32_t w[8];
+    for (int ch = 0; ch < 4; ++ch) {
+        const int32_t col = c0 + ch * 8;
+        if (col >= args.N)
+            break;
+        uint32_t w[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                w[e] = pack_bf16x2(__fmul_rn(__uint_as_float(rr[2 * e]), alpha),
-                                   __fmul_rn(__uint_as_float(rr[2 * e + 1]), alpha));
-            if (edge_chunk(c0 + ch * 16, 16, row0, args)) {
-                const int32_t row = row0 + lane, col = c0 + ch * 16;
-                if (row < args.M) {
-                    uint16_t* dst = static_cast<uint16_t*>(args.d) + (int64_t)row * args.ldd + col;
+        for (int e = 0; e < 8; ++e)
+            w[e] = __float_as_uint(__fmul_rn(__uint_as_float(r[ch * 8 + e]), alpha));
+        if (edge_chunk(col, 8, row0, args)) {
+            const int32_t row = row0 + lane;
+            if (row < args.M) {
+                float* dst = static_cast<float*>(args.d) + (int64_t)row * args.ldd + col;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (col + e < args.N)
-                            dst[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
-                }
-                continue;
+                for (int e = 0; e < 8; ++e)
+                    if (col + e < args.N)
+                        dst[e] = __uint_as_float(w[e]);
             }
-            if (lane == 0)
-                bulk_wait_read0();
-            __syncwarp();
-            reinterpret_cast<uint4*>(buf + lane * 32)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            reinterpret_cast<uint4*>(buf + lane * 32)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_2d(tma_d, buf, c0 + ch * 16, row0);
-                bulk_commit_group();
-            }
+            continue;
         }
+        store_chunk(w, col, row0, buf, tma_d, lane);
     }
 }
 
