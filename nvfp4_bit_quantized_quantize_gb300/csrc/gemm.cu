@@ -227,29 +227,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool live = c0 < args.N && row0 < args.M;
             uint8_t* buf = store_buf + (warp - 2) * kStoreBufBytes;
             const uint32_t taddr = tmem + ((q * 32) << 16) + half * 128;
-            uint32_t p[64];
+            if (args.out_f32) {
+                // binary32 output: each 32-column round goes out before the next load
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + h * 32, r);
-                tmem_ld_wait();
-                if (args.out_f32) {
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + h * 32, r);
+                    tmem_ld_wait();
                     if (live)
                         epilogue_store_f32(r, alpha, row0, c0 + h * 32, args, buf, &tma_d, lane);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        p[h * 16 + e] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * e]), alpha),
-                                                    __fmul_rn(__uint_as_float(r[2 * e + 1]), alpha));
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ctl->tmem_empty);
+            } else {
+                // two rounds of two loads and one wait, packed to bf16 pairs
+                uint32_t p[64];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld_32x32b_x32(taddr + h * 64, ra);
+                    tmem_ld_32x32b_x32(taddr + h * 64 + 32, rb);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        p[h * 32 + e] = pack_bf16x2(__fmul_rn(__uint_as_float(ra[2 * e]), alpha),
+                                                    __fmul_rn(__uint_as_float(ra[2 * e + 1]), alpha));
+                        p[h * 32 + 16 + e] = pack_bf16x2(__fmul_rn(__uint_as_float(rb[2 * e]), alpha),
+                                                         __fmul_rn(__uint_as_float(rb[2 * e + 1]), alpha));
+                    }
+                }
+                // the accumulator is free once every load has landed in registers
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ctl->tmem_empty);
+                if (live)
+                    epilogue_store_bf16(p, row0, c0, args, buf, &tma_d, lane);
             }
-            // the accumulator is free once every load has landed in registers
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&ctl->tmem_empty);
-            if (live && !args.out_f32)
-                epilogue_store_bf16(p, row0, c0, args, buf, &tma_d, lane);
         }
         if (lane == 0)
             bulk_wait_all();

@@ -33,26 +33,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// A 32-row x `width`-column output chunk that crosses the M or N edge is
-// written with plain stores instead of a tensor store, so that nothing outside
-// M x N is touched whatever the tensor unit does with a partial 16-byte unit.
-__device__ __forceinline__ bool edge_chunk(int32_t col, int32_t width, int32_t row0, const GemmArgs& a)
-{
-    return col + width > a.N || row0 + 32 > a.M;
-}
-
 constexpr int kStoreBufBytes = 1024;  // per epilogue warp: 32 rows x 32 bytes
 
-// Send one 32-row x 32-byte chunk (w: this lane's row) through the warp's
-// staging buffer and a TMA tensor store at (col, row0).
-__device__ __forceinline__ void store_chunk(const uint32_t (&w)[8], int32_t col, int32_t row0, uint8_t* buf,
+// Write this lane's 32-byte row (words base .. base + 7 of w) of a 32-row
+// chunk of `width` columns into the warp's staging buffer (after the previous
+// tensor store has read it), then either send the chunk with one TMA tensor
+// store at (col, row0) or, for a chunk crossing the M or N edge, copy each
+// row's elements inside M x N out with plain stores (so nothing outside
+// M x N is touched whatever the tensor unit would do with a partial 16-byte
+// unit).
+template <int kN>
+__device__ __forceinline__ void store_chunk(const uint32_t (&w)[kN], int base, int32_t col, int32_t width,
+                                            int32_t row0, const GemmArgs& args, uint8_t* buf,
                                             const CUtensorMap* tma_d, int lane)
 {
     if (lane == 0)
         bulk_wait_read0();
     __syncwarp();
-    reinterpret_cast<uint4*>(buf + lane * 32)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    reinterpret_cast<uint4*>(buf + lane * 32)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    uint8_t* row = buf + lane * 32;
+    reinterpret_cast<uint4*>(row)[0] = make_uint4(w[base], w[base + 1], w[base + 2], w[base + 3]);
+    reinterpret_cast<uint4*>(row)[1] = make_uint4(w[base + 4], w[base + 5], w[base + 6], w[base + 7]);
+    if (col + width > args.N || row0 + 32 > args.M) {
+        __syncwarp();
+        const int32_t r = row0 + lane;
+        const int es = 32 / width;  // element bytes
+        if (r < args.M) {
+            uint8_t* dst = static_cast<uint8_t*>(args.d) + ((int64_t)r * args.ldd + col) * es;
+#pragma unroll 1
+            for (int e = 0; e < width && col + e < args.N; ++e) {
+                if (es == 2)
+                    reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(row)[e];
+                else
+                    reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(row)[e];
+            }
+        }
+        __syncwarp();
+        return;
+    }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
@@ -63,8 +80,7 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&w)[8], int32_t col,
 
 // Store this warp's 32 rows (row0 + lane) x 128 columns (c0 ..) held as bf16
 // pairs in p (word j: columns c0 + 2j, c0 + 2j + 1, the first in the low
-// half): 16-column chunks leave through TMA tensor stores; chunks on the M/N
-// edge take plain stores of the valid elements.
+// half) as eight 16-column chunks.
 __device__ __forceinline__ void epilogue_store_bf16(const uint32_t (&p)[64], int32_t row0, int32_t c0,
                                                    const GemmArgs& args, uint8_t* buf, const CUtensorMap* tma_d,
                                                    int lane)
@@ -74,52 +90,26 @@ __device__ __forceinline__ void epilogue_store_bf16(const uint32_t (&p)[64], int
         const int32_t col = c0 + ch * 16;
         if (col >= args.N)
             break;
-        uint32_t w[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            w[e] = p[ch * 8 + e];
-        if (edge_chunk(col, 16, row0, args)) {
-            const int32_t row = row0 + lane;
-            if (row < args.M) {
-                uint16_t* dst = static_cast<uint16_t*>(args.d) + (int64_t)row * args.ldd + col;
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    if (col + e < args.N)
-                        dst[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
-            }
-            continue;
-        }
-        store_chunk(w, col, row0, buf, tma_d, lane);
+        store_chunk(p, ch * 8, col, 16, row0, args, buf, tma_d, lane);
     }
 }
 
 // Store 32 rows x 32 columns (c0 ..) of binary32 accumulator values r times
-// alpha, in 8-column chunks, as above.
+// alpha as four 8-column chunks.
 __device__ __forceinline__ void epilogue_store_f32(const uint32_t (&r)[32], float alpha, int32_t row0, int32_t c0,
                                                   const GemmArgs& args, uint8_t* buf, const CUtensorMap* tma_d,
                                                   int lane)
 {
+    uint32_t w[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+        w[e] = __float_as_uint(__fmul_rn(__uint_as_float(r[e]), alpha));
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) {
         const int32_t col = c0 + ch * 8;
         if (col >= args.N)
             break;
-        uint32_t w[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            w[e] = __float_as_uint(__fmul_rn(__uint_as_float(r[ch * 8 + e]), alpha));
-        if (edge_chunk(col, 8, row0, args)) {
-            const int32_t row = row0 + lane;
-            if (row < args.M) {
-                float* dst = static_cast<float*>(args.d) + (int64_t)row * args.ldd + col;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (col + e < args.N)
-                        dst[e] = __uint_as_float(w[e]);
-            }
-            continue;
-        }
-        store_chunk(w, col, row0, buf, tma_d, lane);
+        store_chunk(w, ch * 8, col, 8, row0, args, buf, tma_d, lane);
     }
 }
 
