@@ -277,6 +277,34 @@ def run_e2e(step, args, stream):
     return t0, t1, h2d, d2h
 
 
+def bind_host_to_gpu_node(dev_index: int):
+    """Run this process on the CPUs attached to the GPU (the PCI device's
+    local_cpulist in sysfs), so that the pinned host buffers, which land on
+    the allocating thread's memory node, sit next to the GPU's own host link
+    instead of behind a CPU-to-CPU hop.  Returns the CPU list, or None when
+    sysfs does not give one."""
+    import torch
+
+    p = torch.cuda.get_device_properties(dev_index)
+    path = f"/sys/bus/pci/devices/{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0/local_cpulist"
+    try:
+        txt = open(path).read().strip()
+    except OSError:
+        return None
+    cpus = set()
+    for part in txt.split(","):
+        if "-" in part:
+            lo, hi = part.split("-")
+            cpus.update(range(int(lo), int(hi) + 1))
+        elif part:
+            cpus.add(int(part))
+    cpus &= os.sched_getaffinity(0)
+    if not cpus:
+        return None
+    os.sched_setaffinity(0, cpus)
+    return txt
+
+
 def max_over_ranks(ms: float, world: int, device) -> float:
     """The slowest rank's time: with N replicas the job ends when the last one
     does.  One all-reduce MAX of a single float64 (on `device`: the rank's GPU
@@ -305,6 +333,7 @@ def run_ours(args, rank, world, local_rank):
     build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    host_cpus = bind_host_to_gpu_node(local_rank)
     step = MlpStep(dev)
     launches = step.launches()
     stream = torch.cuda.current_stream(dev)
@@ -420,7 +449,8 @@ def run_ours(args, rank, world, local_rank):
                        "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": round(ms_e2e / args.steps, 4),
                        "note": "pinned host inputs copied in and results copied out every step; copies on "
-                               "separate streams overlap the neighbouring steps' compute (two device slots)"}
+                               "separate streams overlap the neighbouring steps' compute (two device slots)",
+                       "host_cpus": host_cpus}
 
     if not args.no_extras:
         line["extras"] = measure_extras(step, stream, pk)
