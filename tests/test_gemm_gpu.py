@@ -104,6 +104,22 @@ def test_gemm_ragged_shapes(M, N, K):
         _check(d, ref, dabs, not f32, f"ragged {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(8192, 4096, 64), (6000, 2100, 96)])
+def test_gemm_many_tiles_short_k(M, N, K):
+    """One or two K stages per tile and ~14 tiles per CTA: the stage ring,
+    the scale slots and the accumulator hand-over wrap around many times."""
+    rng = np.random.default_rng(M + N + K)
+    qa, sfa = _random_operand(M, K, rng)
+    qb, sfb = _random_operand(N, K, rng)
+    ga, gb = 0.5, 0.25
+    d, st = gemm(qa, sfa, ga, qb, sfb, gb, M, N, K)
+    assert st == 0
+    ms = np.concatenate([rng.integers(0, M, 8192), np.arange(M), np.full(N, M - 1)])
+    ns = np.concatenate([rng.integers(0, N, 8192), np.arange(M) % N, np.arange(N)])
+    ref, dabs = O.gemm_f64_sampled(qa, sfa, ga, qb, sfb, gb, M, N, K, ms, ns)
+    _check(d[ms, ns], ref, dabs, True, f"many tiles {M}x{N}x{K}")
+
+
 def test_ragged_linear_layer_from_quantizers():
     """Quantize X [200, 96] and W [136, 96] with the CUDA quantizers (whose
     scale padding the GEMM relies on) and multiply: Y = X W^T."""
