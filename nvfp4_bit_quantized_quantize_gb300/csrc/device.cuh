@@ -162,8 +162,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     d |= (uint64_t)(swizzle & 7) << 61;
     return d;
 }
-constexpr uint32_t kSwizzleNone = 0;
-constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzle128B = 2;  // swizzle-mode field value for 128-byte swizzle
 
 // D(tmem) (+)= A(smem) x B(smem)^T with E2M1 operands and E4M3 block-16 scales
 // read from tmem.
@@ -189,13 +188,6 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
-}
-
-// Copy a 32-row x 16-byte block of shared memory into tmem, replicated into
-// the four 32-lane quarters (4 columns per lane).
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 __device__ __forceinline__ void tc_commit(uint64_t* bar)

@@ -7,20 +7,21 @@
 // A [M, K] and B [N, K] are packed E2M1 codes (K contiguous) with one E4M3
 // scale per 16 elements in the 128 x 4 atom layout.  Ragged M, N and K are
 // padded on chip: tensor loads past the edges read zeros, the scale buffers'
-// padding (zero, as the quantizers write it) covers the last atoms, and the
-// output tensor store drops rows and columns past M and N.  Each CTA owns a
-// persistent sequence of 128 x 256 output tiles:
+// padding (zero, as the quantizers write it) covers the last atoms, and
+// output chunks that cross M or N are written with plain stores of the
+// elements inside M x N.  Each CTA owns a persistent sequence of 128 x 256
+// output tiles:
 //   warp 0  TMA producer: A/B tiles (128-byte swizzle) and the scale atoms
 //           (3-D tensor boxes of 4 atoms) into a 4-stage shared-memory ring;
 //   warp 1  allocates tensor memory and issues tcgen05.mma.kind::mxf4nvf4
 //           (K = 64 per instruction, binary32 accumulator in tensor memory);
 //   warps 2-9 epilogue, two per tensor-memory lane quarter (128 columns
 //           each): the accumulator read in two rounds of two tcgen05.ld and
-//           one wait, times ga*gb and rounded to bf16 pairs (binary32 output
-//           is stored round by round), the accumulator released, then
-//           32-row chunks staged in a 1 KB shared buffer per warp leave
-//           through TMA bulk tensor stores (per-thread row stores would flood
-//           the memory pipe the MMA warp issues through);
+//           one wait, times ga*gb and rounded to bf16 pairs, the accumulator
+//           released, then 32-row chunks staged in a 1 KB shared buffer per
+//           warp leave through TMA bulk tensor stores (per-thread 16-byte
+//           global stores measured a third slower); binary32 output goes out
+//           in four rounds of one load, each stored before the next;
 //   warps 10-13 one per tensor-memory lane quarter: write each stage's scale
 //           atoms from shared memory into that quarter's lanes with
 //           tcgen05.st (every quarter holds the four 32-row groups of an atom,
