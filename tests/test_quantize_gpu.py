@@ -247,3 +247,23 @@ def test_nonfinite_input_is_reported_by_every_form():
     assert rht_quantize(bb, 0, nv.RN, 0)[3] == 4
     with pytest.raises(O.OracleError):
         O.rht_quantize(bb, 0, O.RN, 0)
+
+
+def test_grid_barrier_time_limit_is_reported():
+    """The grid barrier counts CTA arrivals in word 2 of the workspace, from 0
+    up to the grid size.  Started at 2^32 - 1 the count wraps to one below the
+    grid size, so the barrier can only end by its 2 s time limit: the kernel
+    must finish, report NVFP4_ERR_TIMEOUT, and the workspace must work again
+    after nvfp4_workspace_init.  Nothing faults or hangs."""
+    import torch
+    x = synth.normal_bf16((512, 256), 61, 0)
+    ws = nv.alloc_workspace()
+    ws.view(torch.int32)[2] = -1
+    _, _, _, st = quantize(x, nv.RN, 0, ws=ws)
+    assert st == 5, nv.nvfp4_status_str(st)
+    nv.nvfp4_workspace_init(ws)
+    q, sf, g, st = quantize(x, nv.RN, 0, ws=ws)
+    rq, rsf, rg = O.quantize(x, O.RN, 0)
+    assert st == 0 and g == rg
+    _assert_same(q, rq, "codes after recovery")
+    _assert_same(sf, rsf, "scales after recovery")
