@@ -392,6 +392,27 @@ def test_single_outlier_block_scales():
     assert lin[0, 0] == O.e4m3_rn_sat(float(sbf))
 
 
+def test_all_equal_blocks_round_to_six():
+    # A block of equal values c has bamax = |c|; when its E4M3 scale is a
+    # normal number (448 |c| / amax >= 2^-6) the scale is within 1/16 of
+    # bamax/6 (times s_enc), so c lands within [6/1.0625, 6] or above 6
+    # before rounding, which round-to-nearest (midpoint 5 below, 6 the
+    # largest code) always takes to +-6.  Blocks whose scale falls below the
+    # E4M3 normals are left out (coarser subnormal scales, or zero).
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([rng.uniform(-50, 50, 60), [1.0, -1.0, 2.0 ** -20, 3.0e4]]).astype(np.float32)
+    x = np.repeat(vals, 16).reshape(len(vals), 16)
+    x = np.concatenate([x, np.full((4, 16), 7.0e4, np.float32)])  # the tensor amax
+    xb = synth.f32_to_bf16_bits(x)
+    xs = synth.bf16_bits_to_f32(xb).astype(np.float64)
+    q, sf, g = O.quantize(xb, O.RN)
+    codes = np.stack([q & 15, (q >> 4) & 15], -1).reshape(x.shape)
+    normal = np.abs(xs) * 448.0 / np.abs(xs).max() >= 2.0 ** -6 * 1.01
+    expect = np.where(np.signbit(xs), 0xF, 0x7)
+    assert normal.sum() > 16 * 40
+    assert np.array_equal(codes[normal], expect[normal])
+
+
 def test_quantize_error_bound_and_nearest():
     # The RN result is the nearest grid point to x*f (|.| <= 6) and the
     # dequantized error obeys the half-gap bound of each block.

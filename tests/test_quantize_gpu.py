@@ -267,3 +267,60 @@ def test_grid_barrier_time_limit_is_reported():
     assert st == 0 and g == rg
     _assert_same(q, rq, "codes after recovery")
     _assert_same(sf, rsf, "scales after recovery")
+
+
+def _edge_value_tensor(rows, cols, seed):
+    """Blocks of the method's edge cases, tiled over the tensor: all-equal
+    blocks of both signs, one outlier among zeros, one outlier among tiny
+    values, alternating +-amax, bf16 subnormals, values at the E2M1 grid
+    points of their block scale, and plain N(0, 1)."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    blocks = x.reshape(rows, cols // 16, 16)
+    kinds = rng.integers(0, 7, (rows, cols // 16))
+    for r in range(rows):
+        for b in range(cols // 16):
+            k = kinds[r, b]
+            v = blocks[r, b]
+            if k == 0:
+                v[:] = rng.choice([-1, 1]) * rng.uniform(0.1, 100)
+            elif k == 1:
+                v[:] = 0.0
+                v[rng.integers(16)] = rng.choice([-1, 1]) * rng.uniform(1, 1000)
+            elif k == 2:
+                v[:] = rng.uniform(-1e-6, 1e-6, 16)
+                v[rng.integers(16)] = 50.0
+            elif k == 3:
+                v[:] = np.where(np.arange(16) % 2 == 0, 3.0, -3.0)
+            elif k == 4:
+                v[:] = rng.uniform(-1, 1, 16) * 2.0 ** -130
+            elif k == 5:
+                v[:] = rng.choice([0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], 16) * rng.choice([-1, 1], 16) * 0.25
+    return synth.f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("mode", [nv.RN, nv.SR])
+def test_edge_value_blocks_every_form(mode):
+    x = _edge_value_tensor(256, 384, 71)
+    q, sf, g, st = quantize(x, mode, seed=9)
+    rq, rsf, rg = O.quantize(x, mode, 9)
+    assert st == 0 and g == rg
+    _assert_same(q, rq, "1x16 codes")
+    _assert_same(sf, rsf, "1x16 scales")
+    qT, sfT, gT, st = rht_quantize(x, 4, mode, 10)
+    rqT, rsfT, rgT = O.rht_quantize(x, 4, mode, 10)
+    assert st == 0 and gT == rgT
+    _assert_same(qT, rqT, "rht codes")
+    _assert_same(sfT, rsfT, "rht scales")
+    q, sf, g, qT, sfT, gT, st = quantize_dual(x, mode, 9, 4, mode, 10)
+    assert st == 0 and g == rg and gT == rgT
+    _assert_same(q, rq, "dual row codes")
+    _assert_same(qT, rqT, "dual rht codes")
+    if mode == nv.RN:
+        q, sf, qT2, sfT2, g, st = quantize_2d(x)
+        rq2, rsf2, rqT2, rsfT2, rg2 = O.quantize_2d(x)
+        assert st == 0 and g == rg2
+        _assert_same(q, rq2, "2-D codes")
+        _assert_same(sf, rsf2, "2-D scales")
+        _assert_same(qT2, rqT2, "2-D transposed codes")
+        _assert_same(sfT2, rsfT2, "2-D transposed scales")
