@@ -89,3 +89,16 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.nvfp4_quantize_dual(fake, 32, 32, 32, 0, 0, fake, fake, fake, 1, 1, 0, None, fake, fake, fake,
                                  None) == 1
     assert L.nvfp4_workspace_init(None, None) == 1
+    # noise meter: cols % 16, 8-byte aligned sums
+    assert L.nvfp4_quant_noise(fake, 16, 24, 24, fake, fake, fake, fake, None) == 2
+    assert L.nvfp4_quant_noise(fake, 16, 32, 32, fake, fake, fake, fake + 4, None) == 3
+    assert L.nvfp4_quant_noise(fake, 16, 32, 32, None, fake, fake, fake, None) == 1
+    # MXFP4: 32-element blocks; its GEMM has the same shape rules as NVFP4's
+    assert L.nvfp4_mxfp4_quantize(fake, 16, 48, 48, fake, fake, fake, None) == 2
+    assert L.nvfp4_mxfp4_quantize(fake, 16, 64, 64, fake, fake, None, None) == 1
+    assert L.nvfp4_mxfp4_gemm(fake, fake, fake, fake, 128, 128, 80, fake, 128, 0, fake, None) == 2
+    assert L.nvfp4_mxfp4_gemm(fake, fake, fake, fake, 128, 128, 64, fake, 132, 0, fake, None) == 3
+    # allocation-free quantizer: mode, shape, alignment
+    assert L.nvfp4_quantize_noalloc(fake, 16, 16, 16, 5, 0, fake, fake, fake, None) == 1
+    assert L.nvfp4_quantize_noalloc(fake, 16, 24, 24, 0, 0, fake, fake, fake, None) == 2
+    assert L.nvfp4_quantize_noalloc(fake + 8, 16, 16, 16, 0, 0, fake, fake, fake, None) == 3
