@@ -31,8 +31,10 @@
  * fast-math.  The matmul accumulates in binary64.
  *
  * Parity status per function:
- *  - e2m1/e4m3 codecs, quantizers, RHT, swizzle, GEMM: pinned by the CPU tests
- *    (tables from the pages, closed forms, invariants, brute force).
+ *  - e2m1/e4m3 codecs, quantizers (1x16, 2-D, RHT), stochastic rounding,
+ *    scale layout, GEMM, noise meter, MXFP4 quantizer and GEMM: pinned by the
+ *    CPU tests (tables from the pages, closed forms, invariants, brute force,
+ *    hand-worked examples).
  *  - philox4x32_10: the exact bit stream is "parity unpinned" (no published
  *    known-answer values are used); its statistics are pinned.
  */
