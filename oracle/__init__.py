@@ -8,9 +8,9 @@ transform, stochastic rounding).  Only the tests, ``__graft_entry__.smoke()``
 and the CPU-baseline leg of ``bench.py`` may import this package.  The library
 path never does, and this package imports nothing from the library.
 
-Parity status: every function is pinned by ``tests/test_oracle_*.py`` except the
-exact bit stream of the Philox generator ("parity unpinned"; its statistics are
-pinned).
+Parity status: every function is pinned by ``tests/test_oracle_pins.py``,
+including the Philox generator's exact bit stream (the known-answer vectors
+published with the method).
 """
 from __future__ import annotations
 

@@ -30,13 +30,14 @@
  * time, in the order written here.  Build with -ffp-contract=off and without
  * fast-math.  The matmul accumulates in binary64.
  *
- * Parity status per function:
- *  - e2m1/e4m3 codecs, quantizers (1x16, 2-D, RHT), stochastic rounding,
- *    scale layout, GEMM, noise meter, MXFP4 quantizer and GEMM: pinned by the
- *    CPU tests (tables from the pages, closed forms, invariants, brute force,
- *    hand-worked examples).
- *  - philox4x32_10: the exact bit stream is "parity unpinned" (no published
- *    known-answer values are used); its statistics are pinned.
+ * Parity status per function: every function here is pinned by the CPU
+ * tests -- e2m1/e4m3 codecs, quantizers (1x16, 2-D, RHT), stochastic
+ * rounding, scale layout, GEMM, noise meter, MXFP4 quantizer and GEMM by
+ * tables from the pages, closed forms, invariants, brute force and
+ * hand-worked examples; philox4x32_10 by the known-answer vectors published
+ * with the method (Salmon et al., SC'11); sr_values by hand-derived values of
+ * one block from those vectors and a decision-independence test of the
+ * elements that share a word; rht_signs by its word, bit range and counter.
  */
 #include <stdint.h>
 #include <stddef.h>

@@ -154,6 +154,68 @@ def test_sr_values_are_uniform_16_bit_and_use_each_word_twice():
             assert sum(pop(v[4 * m + i]) for i in range(4)) == 2 * pop(w[m])
 
 
+def test_sr_values_of_block_0_seed_0_by_hand():
+    # Philox4x32-10, key (0, 0), counter (0, 0, 0, 0) is the first published
+    # known-answer vector: words 6627E8D5 E169C58D BC57AC4C 9B00DBD8.  Word 0's
+    # bytes, least significant first, are b0 = D5, b1 = E8, b2 = 27, b3 = 66.
+    # The reading pairs them as
+    #   element 0: b2 b0            = 27 D5 = 10197
+    #   element 1: rev(b0) rev(b2)  = AB E4 = 44004   (rev(D5) = AB, rev(27) = E4)
+    #   element 2: b3 b1            = 66 E8 = 26344
+    #   element 3: rev(b1) rev(b3)  = 17 66 = 5990    (rev(E8) = 17, rev(66) = 66)
+    # and word 1 = E169C58D (b0 = 8D, b1 = C5, b2 = 69, b3 = E1) gives
+    #   element 4: 69 8D = 27021, element 5: B1 96 = 45462,
+    #   element 6: E1 C5 = 57797, element 7: A3 87 = 41863.
+    R = O.sr_values(0, 0)
+    assert [int(v) for v in R[:8]] == [0x27D5, 0xABE4, 0x66E8, 0x1766, 0x698D, 0xB196, 0xE1C5, 0xA387]
+    # the block index is the counter: block (2^32 + 3) uses counter (3, 1, 0, 0)
+    w = O.philox4x32_10([3, 1, 0, 0], [9, 0])
+    b = [(int(w[2]) >> (8 * i)) & 0xFF for i in range(4)]
+    rev = lambda x: int(f"{x:08b}"[::-1], 2)
+    assert [int(v) for v in O.sr_values(9, (1 << 32) + 3)[8:12]] == [
+        b[2] * 256 + b[0], rev(b[0]) * 256 + rev(b[2]), b[3] * 256 + b[1], rev(b[1]) * 256 + rev(b[3])]
+
+
+def test_sr_paired_elements_round_independently():
+    # Elements 4m and 4m+1 (and 4m+2, 4m+3) draw their 16-bit values from the
+    # same two bytes of one Philox word, once in each order and bit-reversed.
+    # Their up/down decisions must still be uncorrelated: over 2^17 blocks of
+    # the full quantizer, with fractions of 16 significant bits, the
+    # covariance of the decisions of each such pair is within 4 sigma of 0.
+    n = 1 << 17
+    # block max 5.5 under tensor max 6: scale byte 416, f = rn(448/416) is not
+    # a power of two, so every scaled element carries a fraction with (at
+    # least) 16 significant bits between its grid neighbours
+    row = np.array([5.5, 1.25, 0.75, 3.0, 1.75, 2.5, 0.375, 4.5,
+                    1.125, 0.625, 2.25, 3.5, 0.875, 1.375, 2.75, 5.0], np.float32)
+    x = np.tile(row, (n, 1))
+    x[0, :] = 6.0
+    xb = synth.f32_to_bf16_bits(x)
+    q, sf, g = O.quantize(xb, O.SR, 12345)
+    assert sf[O.sf_offset(1, 0, 1)] == O.e4m3_rn_sat(416.0)
+    f = np.float32(448.0) / np.float32(416.0)
+    v = (row * f).astype(np.float32)
+    lo = np.array([max(m for m in PAGE_E2M1_MAGNITUDES if m <= a) for a in v])
+    gap = np.array([0.5 if a < 2 else (1.0 if a < 4 else 2.0) for a in v])
+    t = np.floor((v - lo) / gap * 65536.0)
+    # strictly between grid points, and not on a 2^-8 step of the gap: the
+    # decisions depend on both bytes of each element's random value
+    assert np.all((t > 0) & (t < 65536) & (t % 256 != 0)), t
+    codes = np.empty((n, 16), np.int64)
+    codes[:, 0::2] = q & 15
+    codes[:, 1::2] = q >> 4
+    mags = np.array(PAGE_E2M1_MAGNITUDES)[codes[1:] & 7]
+    up = (mags > lo).astype(np.float64)
+    # marginal probability is the kept fraction (16 bits) of the gap
+    p = up.mean(axis=0)
+    sig_p = np.sqrt(t / 65536 * (1 - t / 65536) / (n - 1))
+    assert np.all(np.abs(p - t / 65536) <= 4 * sig_p + 1e-12), (p, t / 65536)
+    for a, b in [(4 * m + i, 4 * m + i + 1) for m in range(4) for i in (0, 2)]:
+        cov = np.mean((up[:, a] - p[a]) * (up[:, b] - p[b]))
+        sigma = math.sqrt(p[a] * (1 - p[a]) * p[b] * (1 - p[b]) / (n - 1))
+        assert abs(cov) <= 4 * sigma, (a, b, cov, sigma)
+
+
 def test_sr_unbiased_over_seeds_through_quantize():
     # Statistical pin through the full quantizer: the mean over many seeds of
     # the dequantized SR result matches the closed form within 4 sigma.
@@ -215,9 +277,29 @@ def test_e4m3_saturation_and_golden():
 
 # --------------------------------------------------------------- Philox ----
 
+# Known-answer vectors of Philox4x32 with 10 rounds, as published with the
+# method (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1,
+# 2, 3", SC'11): (counter words, key words) -> output words.
+PHILOX4x32_10_KAT = [
+    ((0x00000000, 0x00000000, 0x00000000, 0x00000000), (0x00000000, 0x00000000),
+     (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+    ((0xFFFFFFFF, 0xFFFFFFFF, 0xFFFFFFFF, 0xFFFFFFFF), (0xFFFFFFFF, 0xFFFFFFFF),
+     (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+    ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+     (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1)),
+]
+
+
+@pytest.mark.parametrize("ctr,key,out", PHILOX4x32_10_KAT)
+def test_philox_known_answer_vectors(ctr, key, out):
+    # the generator's exact bit stream: round multipliers, Weyl key schedule,
+    # word order and the number of rounds all show in these three vectors
+    assert [int(w) for w in O.philox4x32_10(list(ctr), list(key))] == list(out)
+
+
 def test_philox_statistics():
-    # parity unpinned for the exact stream; pin uniformity and counter/key
-    # sensitivity of the bytes used for stochastic rounding.
+    # uniformity and counter/key sensitivity of the bytes used for stochastic
+    # rounding (the exact stream is pinned by the known-answer vectors above)
     words = np.array([O.philox4x32_10([i, 0, 0, 0], [1234, 0]) for i in range(20000)], np.uint32)
     b = words.view(np.uint8).ravel()
     counts = np.bincount(b, minlength=256)
@@ -287,6 +369,26 @@ def test_rht_signs_use_16_bits():
     seen = {O.rht_signs(s) for s in range(64)}
     assert all(0 <= x < (1 << 16) for x in seen)
     assert len(seen) > 60
+
+
+def test_rht_signs_are_the_low_16_bits_of_word_0_at_counter_0010():
+    # Reading: the sign diagonal of seed s is bits 0..15 of word 0 of
+    # Philox4x32-10 with key (s lo, s hi) and counter (0, 0, 1, 0); a set bit
+    # i negates input i.  The generator itself is pinned by the known-answer
+    # vectors, so this fixes the word, the bit range and the counter.
+    for seed in (0, 1, 5, 0xDEADBEEF, (7 << 32) | 3):
+        w = O.philox4x32_10([0, 0, 1, 0], [seed & 0xFFFFFFFF, seed >> 32])
+        assert O.rht_signs(seed) == int(w[0]) & 0xFFFF, seed
+        # not word 1, not the high half, not counter (0, 0, 0, 0)
+        assert O.rht_signs(seed) != int(w[1]) & 0xFFFF or O.rht_signs(seed) == 0
+    # seed 0: word 0 is 0x????15E1 -> inputs 0, 5, 6, 7, 8, 10 and 12 are negated
+    assert O.rht_signs(0) == 0x15E1
+    assert O.rht_signs(0) != int(O.philox4x32_10([0, 0, 0, 0], [0, 0])[0]) & 0xFFFF
+    e = np.eye(16, dtype=np.float32)
+    cols = np.stack([O.rht16(e[i], 0x15E1) for i in range(16)])
+    plain = np.stack([O.rht16(e[i], 0) for i in range(16)])
+    negated = [i for i in range(16) if np.array_equal(cols[i], -plain[i])]
+    assert negated == [0, 5, 6, 7, 8, 10, 12]
 
 
 # --------------------------------------------------------- swizzled layout ----
