@@ -39,6 +39,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+from nvfp4_bit_quantized_quantize_gb300.step import MlpStep  # noqa: E402  (torch-free at import)
+
 WORKLOAD = "mlp7b_fwd_bwd_h4096_f11008_t8192"
 TOKENS, HIDDEN, FFN = 8192, 4096, 11008
 GEMM_FLOPS = 2.0 * TOKENS * HIDDEN * FFN
@@ -149,16 +151,9 @@ class ClockSampler:
 
 # --------------------------------------------------------------- our arm ----
 
-class MlpStep:
-    """Device buffers and the 12 launches of one fwd+bwd step.
-
-    Inputs (X, W_up, W_down, dY_down) and results (Y, dX, dW_up, dW_down) have
-    two device slots, so that the end-to-end leg can copy the next step's
-    inputs in and the previous step's results out while a step computes;
-    intermediates (quantized operands, H, dH) are shared."""
-
-    IN = ("X", "W_up", "W_down", "dY_down")
-    OUT = ("Y", "dX", "dW_up", "dW_down")
+class BenchStep(MlpStep):
+    """The package's MlpStep at the 7B-MLP shape with two slots of inputs and
+    results, plus pinned host copies of both for the end-to-end leg."""
 
     def __init__(self, dev):
         import numpy as np
@@ -167,71 +162,28 @@ class MlpStep:
         import nvfp4_bit_quantized_quantize_gb300 as nv
         from nvfp4_bit_quantized_quantize_gb300 import synth
 
-        self.nv, self.torch = nv, torch
-        self.dev = dev
+        seed = synth.WORKLOADS[WORKLOAD]["seed"]
+        super().__init__(TOKENS, HIDDEN, FFN, seed, dev, slots=2)
+        self.nv, self.dev = nv, dev
         host = synth.make_workload(WORKLOAD)
-        self.seed = synth.WORKLOADS[WORKLOAD]["seed"]
         bf = torch.bfloat16
-        T, D, F = TOKENS, HIDDEN, FFN
-        e = lambda *s: torch.empty(s, dtype=bf, device=dev)
-        # pinned host inputs, and two device slots of inputs and results
         self.h_in = {k: torch.from_numpy(host[k].view(np.int16)).view(bf).pin_memory() for k in self.IN}
-        self.d_in = [{k: v.to(dev) for k, v in self.h_in.items()} for _ in range(2)]
-        shapes = {"Y": (T, D), "dX": (T, D), "dW_up": (F, D), "dW_down": (D, F)}
-        self.d_out = [{k: e(*shp) for k, shp in shapes.items()} for _ in range(2)]
-        self.h_out = [{k: torch.empty(shp, dtype=bf).pin_memory() for k, shp in shapes.items()} for _ in range(2)]
-        self.H, self.dH = e(T, F), e(T, F)
-        q = lambda r, c: nv.alloc_quantized(r, c, dev)
-        self.xq, self.wuq, self.wuqT = q(T, D), q(F, D), q(D, F)
-        self.hq, self.wdq, self.wdqT = q(T, F), q(D, F), q(F, D)
-        self.dyq, self.dyT, self.hT = q(T, D), q(D, T), q(F, T)
-        self.dhq, self.dhT, self.xT = q(T, F), q(F, T), q(D, T)
-        self.ws = nv.alloc_workspace(dev)
+        for slot in self.inputs:
+            for k, v in self.h_in.items():
+                slot[k].copy_(v)
+        self.h_out = [{k: torch.empty(v.shape, dtype=bf).pin_memory() for k, v in slot.items()}
+                      for slot in self.outputs]
         torch.cuda.synchronize(dev)
-
-    def launches(self, slot=0):
-        nv = self.nv
-        din, dout = self.d_in[slot], self.d_out[slot]
-        x, wu, wd, dy = din["X"], din["W_up"], din["W_down"], din["dY_down"]
-        Y, dX, dW_up, dW_down = dout["Y"], dout["dX"], dout["dW_up"], dout["dW_down"]
-        T, D, F = TOKENS, HIDDEN, FFN
-        ws, s = self.ws, self.seed
-        rht_seed = s + 1
-        Q2 = nv.nvfp4_quantize_2d
-        QD = nv.nvfp4_quantize_dual
-
-        def G(a, b, d, M, N, K):
-            return lambda: nv.nvfp4_gemm(a[0], a[1], a[2], b[0], b[1], b[2], M, N, K, d, N, nv.OUT_BF16, ws)
-
-        def dual(x, C, rows_q, t_q, mode, seed, seed_t):
-            return lambda: QD(x, T, C, C, mode, seed, *rows_q, rht_seed, mode, seed_t, *t_q, ws)
-
-        return [
-            ("quantize_dual", ("rn", T, D), dual(x, D, self.xq, self.xT, nv.RN, 0, 0)),
-            ("quantize_2d_t", ("rn", F, D), lambda: Q2(wu, F, D, D, self.wuq[0], self.wuq[1], self.wuqT[0],
-                                                       self.wuqT[1], self.wuq[2], ws)),
-            ("gemm", (T, F, D), G(self.xq, self.wuq, self.H, T, F, D)),
-            ("quantize_dual", ("rn", T, F), dual(self.H, F, self.hq, self.hT, nv.RN, 0, 0)),
-            ("quantize_2d_t", ("rn", D, F), lambda: Q2(wd, D, F, F, self.wdq[0], self.wdq[1], self.wdqT[0],
-                                                       self.wdqT[1], self.wdq[2], ws)),
-            ("gemm", (T, D, F), G(self.hq, self.wdq, Y, T, D, F)),
-            ("quantize_dual", ("sr", T, D), dual(dy, D, self.dyq, self.dyT, nv.SR, s * 16 + 3, s * 16 + 4)),
-            ("gemm", (T, F, D), G(self.dyq, (self.wdqT[0], self.wdqT[1], self.wdq[2]), self.dH, T, F, D)),
-            ("gemm", (D, F, T), G(self.dyT, self.hT, dW_down, D, F, T)),
-            ("quantize_dual", ("sr", T, F), dual(self.dH, F, self.dhq, self.dhT, nv.SR, s * 16 + 5, s * 16 + 6)),
-            ("gemm", (T, D, F), G(self.dhq, (self.wuqT[0], self.wuqT[1], self.wuq[2]), dX, T, D, F)),
-            ("gemm", (F, D, T), G(self.dhT, self.xT, dW_up, F, D, T)),
-        ]
 
     def h2d(self, slot):
         for k, v in self.h_in.items():
-            self.d_in[slot][k].copy_(v, non_blocking=True)
+            self.inputs[slot][k].copy_(v, non_blocking=True)
         return sum(v.numel() * 2 for v in self.h_in.values())
 
     def d2h(self, slot):
-        for k, v in self.d_out[slot].items():
+        for k, v in self.outputs[slot].items():
             self.h_out[slot][k].copy_(v, non_blocking=True)
-        return sum(v.numel() * 2 for v in self.d_out[slot].values())
+        return sum(v.numel() * 2 for v in self.outputs[slot].values())
 
 
 def run_e2e(step, args, stream):
@@ -264,8 +216,8 @@ def run_e2e(step, args, stream):
             in_ready[sl].record(h2d_s)
         stream.wait_event(in_ready[sl])
         stream.wait_event(out_free[sl])
-        for _, _, fn in lists[sl]:
-            fn()
+        for l in lists[sl]:
+            l.fn()
         in_free[sl].record(stream)
         out_ready[sl].record(stream)
         with torch.cuda.stream(d2h_s):
@@ -275,6 +227,37 @@ def run_e2e(step, args, stream):
     stream.wait_stream(d2h_s)
     t1.record(stream)
     return t0, t1, h2d, d2h
+
+
+def link_rates(step, stream, reps=5):
+    """The host link alone, in the same run: one step's input copies (pinned
+    host -> device) and result copies (device -> pinned host), each direction
+    timed by itself on its own stream (median of `reps`).  The pipelined
+    end-to-end step cannot beat max(h2d, d2h, device step)."""
+    import torch
+
+    dev = step.dev
+    s = torch.cuda.Stream(dev)
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps + 1):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                a.record(s)
+                n = fn()
+                b.record(s)
+            s.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts[1:]), n
+
+    h_ms, h_bytes = timed(lambda: step.h2d(0))
+    d_ms, d_bytes = timed(lambda: step.d2h(0))
+    stream.wait_stream(s)
+    return {"h2d_ms": round(h_ms, 4), "h2d_gbs": round(h_bytes / (h_ms * 1e-3) / 1e9, 1),
+            "d2h_ms": round(d_ms, 4), "d2h_gbs": round(d_bytes / (d_ms * 1e-3) / 1e9, 1),
+            "how": "one step's pinned copies per direction, alone, median of 5 (cudaMemcpyAsync per buffer)"}
 
 
 def bind_host_to_gpu_node(dev_index: int):
@@ -334,7 +317,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     host_cpus = bind_host_to_gpu_node(local_rank)
-    step = MlpStep(dev)
+    step = BenchStep(dev)
     launches = step.launches()
     stream = torch.cuda.current_stream(dev)
 
@@ -344,8 +327,8 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
 
     for _ in range(args.warmup):
-        for _, _, fn in launches:
-            fn()
+        for l in launches:
+            l.fn()
     st = step.nv.nvfp4_device_status(step.ws)
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {step.nv.nvfp4_status_str(st)}")
@@ -362,9 +345,9 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     t0.record(stream)
     for k in range(args.steps):
-        for (_, _, fn), (a, b) in zip(launches, evs[k]):
+        for l, (a, b) in zip(launches, evs[k]):
             a.record(stream)
-            fn()
+            l.fn()
             b.record(stream)
     t1.record(stream)
     barrier()
@@ -376,8 +359,8 @@ def run_ours(args, rank, world, local_rank):
 
     per_kind = {}
     for k in range(args.steps):
-        for (kind, shape, _), (a, b) in zip(launches, evs[k]):
-            per_kind.setdefault((kind, shape), []).append(a.elapsed_time(b))
+        for l, (a, b) in zip(launches, evs[k]):
+            per_kind.setdefault((l.kind, l.shape), []).append(a.elapsed_time(b))
     ms_step = ms_total / args.steps
     flops_step = N_GEMMS * GEMM_FLOPS
     value = job_tflops(world, flops_step, ms_step)
@@ -445,12 +428,14 @@ def run_ours(args, rank, world, local_rank):
         st = step.nv.nvfp4_device_status(step.ws)
         if st != 0:
             raise RuntimeError(f"device status after end-to-end steps: {step.nv.nvfp4_status_str(st)}")
+        link = link_rates(step, stream)
+        link["bound_ms_per_step"] = round(max(link["h2d_ms"], link["d2h_ms"], ms_step), 4)
         line["e2e"] = {"value": round(job_tflops(world, flops_step, ms_e2e / args.steps), 2),
                        "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": round(ms_e2e / args.steps, 4),
                        "note": "pinned host inputs copied in and results copied out every step; copies on "
                                "separate streams overlap the neighbouring steps' compute (two device slots)",
-                       "host_cpus": host_cpus}
+                       "host_cpus": host_cpus, "link": link}
 
     if not args.no_extras:
         line["extras"] = measure_extras(step, stream, pk)
@@ -521,6 +506,26 @@ def measure_configs(step, stream, pk):
         tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
         return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / fp4_peak, 3)}
 
+    # tiny linear layer (X, W 256x256, N(0,1) with 0.5% x50, seed 0): two RN
+    # quantizations and the 256^3 GEMM; latency-bound, reported, not graded
+    import numpy as np
+
+    from nvfp4_bit_quantized_quantize_gb300 import synth
+    wl = synth.make_workload("tiny_linear_256")
+    n1 = 256
+    X1, W1 = (torch.from_numpy(wl[k].view(np.int16)).to(dev).view(torch.bfloat16) for k in ("X", "W"))
+    xq1, wq1 = nv.alloc_quantized(n1, n1, dev), nv.alloc_quantized(n1, n1, dev)
+    d1 = torch.empty((n1, n1), dtype=torch.bfloat16, device=dev)
+    qx = lambda: nv.nvfp4_quantize(X1, n1, n1, n1, nv.RN, 0, *xq1, ws)
+    qw = lambda: nv.nvfp4_quantize(W1, n1, n1, n1, nv.RN, 0, *wq1, ws)
+    g1 = lambda: nv.nvfp4_gemm(*xq1, *wq1, n1, n1, n1, d1, n1, nv.OUT_BF16, ws)
+    out["tiny_linear_256/quantize_1x16[rnx256x256]"] = qline("quantize_1x16", n1, n1, _flushed_ms(qx, stream, flush))
+    out["tiny_linear_256/gemm[256x256x256]"] = gline(n1, n1, n1, _flushed_ms(g1, stream, flush))
+    ms = _flushed_ms(lambda: (qx(), qw(), g1()), stream, flush)
+    out["tiny_linear_256/layer[3 launches]"] = {"ms": round(ms, 4), "note": "quantize X, quantize W, GEMM; "
+                                                "latency-bound (reported, not graded)"}
+    del X1, W1, xq1, wq1, d1
+
     gen = torch.Generator(device=dev)
     gen.manual_seed(1)
     for n in (1024, 4096, 8192):
@@ -584,6 +589,14 @@ def measure_extras(step, stream, pk):
     out["quant_noise[8192x11008]"] = {"ms": round(ms, 4), "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
                                       "frac": round(byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
                                       "norm_ratio": round(float((sums[1] / sums[0]).sqrt()), 3)}
+    # binary32 output (the strict-check form) on the up-projection Fprop operands
+    d32 = torch.empty((T, F), dtype=torch.float32, device=dev)
+    ms = _event_ms(lambda: nv.nvfp4_gemm(*step.xq, *step.wuq, T, F, D, d32, F, nv.OUT_F32, step.ws), stream)
+    out["gemm_f32_out[8192x11008x4096]"] = {"ms": round(ms, 4),
+                                             "TFLOP/s": round(GEMM_FLOPS / (ms * 1e-3) / 1e12, 1),
+                                             "frac": round(GEMM_FLOPS / (ms * 1e-3) / 1e12
+                                                           / (pk["bf16_tflops"] * FP4_OVER_BF16), 3)}
+    del d32
     # ragged GEMM: every dimension off the tile grid
     M, N, K = 8000, 11000, 4064
     a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev)
@@ -608,8 +621,8 @@ def measure_extras(step, stream, pk):
           torch.empty((nv.nvfp4_sf_bytes(T, D),), dtype=torch.uint8, device=dev))
     wb = (torch.empty((F, D // 2), dtype=torch.uint8, device=dev),
           torch.empty((nv.nvfp4_sf_bytes(F, D),), dtype=torch.uint8, device=dev))
-    nv.nvfp4_mxfp4_quantize(step.d_in[0]["X"], T, D, D, xa[0], xa[1], step.ws)
-    nv.nvfp4_mxfp4_quantize(step.d_in[0]["W_up"], F, D, D, wb[0], wb[1], step.ws)
+    nv.nvfp4_mxfp4_quantize(step.inputs[0]["X"], T, D, D, xa[0], xa[1], step.ws)
+    nv.nvfp4_mxfp4_quantize(step.inputs[0]["W_up"], F, D, D, wb[0], wb[1], step.ws)
     ms = _event_ms(lambda: nv.nvfp4_mxfp4_gemm(xa[0], xa[1], wb[0], wb[1], T, F, D, step.H, F, nv.OUT_BF16,
                                                step.ws), stream)
     out["mxfp4_gemm[8192x11008x4096]"] = {"ms": round(ms, 4),
@@ -633,10 +646,23 @@ def measure_extras(step, stream, pk):
 
 # ------------------------------------------------------- CPU oracle arm ----
 
-def oracle_step_estimate(budget_s: float):
+def host_cores() -> int:
+    """Host CPUs this process may run on (the affinity mask; nproc's count)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_step_estimate(budget_s: float, threads: int = 1):
     """Time the oracle on bounded samples of every kind of launch of the step
     (each sample sized to about a fifth of budget_s) and extrapolate the time of
-    one full step.  Returns (seconds, sample description)."""
+    one full step.  With threads > 1 every sample runs as `threads` row slices
+    at once, one oracle call per host thread (the oracle's C code runs outside
+    the interpreter lock), and the per-element time is the wall time over all
+    slices.  Returns (seconds, sample description, samples timed)."""
+    import concurrent.futures as cf
+
     import numpy as np
 
     import oracle as O
@@ -644,17 +670,24 @@ def oracle_step_estimate(budget_s: float):
 
     T, D, F = TOKENS, HIDDEN, FFN
     share = budget_s / 5.0
+    pool = cf.ThreadPoolExecutor(threads) if threads > 1 else None
+    timed = [0]
 
     def per_unit(make, run, units, lo=1):
-        """Grow the sample until one run takes about `share` seconds."""
+        """Grow the sample until one run (of `threads` slices) takes about
+        `share` seconds."""
         n = lo
         while True:
-            arg = make(n)
+            args_ = [make(n) for _ in range(threads)]
             t = time.perf_counter()
-            run(arg)
+            if pool is None:
+                run(args_[0])
+            else:
+                list(pool.map(run, args_))
             dt = time.perf_counter() - t
+            timed[0] += 1
             if dt >= share * 0.5 or n >= (1 << 20):
-                return dt / units(n), n
+                return dt / (units(n) * threads), n
             n = max(n * 2, int(n * share / max(dt, 1e-4) * 0.9))
 
     rng = np.random.default_rng(0)
@@ -671,46 +704,152 @@ def oracle_step_estimate(budget_s: float):
     t_mac, n_out = per_unit(lambda n: (np.arange(n) % 64, (np.arange(n) * 7) % 64),
                             lambda mn: O.gemm_f64_sampled(qa, sa, 1.0, qa, sa, 1.0, 64, 64, K, mn[0], mn[1]),
                             lambda n: n * K, 8)
+    if pool is not None:
+        pool.shutdown()
 
     el = lambda r, c: r * c
     quant = (t_rn * (el(T, D) + el(T, F)) + t_sr * (el(T, D) + el(T, F)) + t_2d * (el(F, D) + el(D, F))
              + t_rht * (el(T, D) * 2 + el(T, F) * 2))
     total = quant + t_mac * (N_GEMMS * GEMM_FLOPS / 2)
-    sample = (f"oracle timed on {r_rn}x{D} (1x16 RN), {r_sr}x{D} (1x16 SR), {16 * r_2d}x{D} (2-D), "
-              f"{T}x{8 * c_rht} (RHT+SR) slices and {n_out} GEMM outputs at K={K}; per-element and "
-              f"per-MAC times extrapolated to the full step ({N_GEMMS} GEMMs; the 1x16, Hadamard and "
-              f"2-D quantizations of the step's 4 dual and 2 weight launches)")
-    return total, sample
+    per = f"{threads} x " if threads > 1 else ""
+    sample = (f"oracle timed on {per}{r_rn}x{D} (1x16 RN), {per}{r_rn}x{D} (1x16 SR), {per}{16 * r_2d}x{D} "
+              f"(2-D), {per}{T}x{8 * c_rht} (RHT+SR) slices and {per}{n_out} GEMM outputs at K={K}; "
+              f"per-element and per-MAC times extrapolated to the full step ({N_GEMMS} GEMMs; the 1x16, "
+              f"Hadamard and 2-D quantizations of the step's 4 dual and 2 weight launches)")
+    return total, sample, timed[0]
 
 
 def cpu_baseline(budget_s: float = 15.0):
+    """The oracle on one host thread (the headline `value`, `cores` = 1) and
+    on every host core (`all_cores`), each on bounded samples of the step."""
     t = time.perf_counter()
-    est, sample = oracle_step_estimate(budget_s)
+    est, sample, _ = oracle_step_estimate(budget_s)
     wall = time.perf_counter() - t
-    return {"value": N_GEMMS * GEMM_FLOPS / est / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": sample + f" (measured in {wall:.1f} s, single thread)",
-            "extrapolated_step_s": round(est, 1)}
+    ncores = host_cores()
+    out = {"value": N_GEMMS * GEMM_FLOPS / est / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+           "sample": sample + f" (measured in {wall:.1f} s, single thread)",
+           "extrapolated": True, "extrapolated_step_s": round(est, 1), "host_nproc": ncores}
+    if ncores > 1:
+        t = time.perf_counter()
+        est_n, sample_n, _ = oracle_step_estimate(budget_s, threads=ncores)
+        wall = time.perf_counter() - t
+        out["all_cores"] = {"value": N_GEMMS * GEMM_FLOPS / est_n / 1e12, "unit": "TFLOP/s", "cores": ncores,
+                            "sample": sample_n + f" (measured in {wall:.1f} s, {ncores} threads)",
+                            "extrapolated_step_s": round(est_n, 1)}
+    return out
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle on this host, one thread.  Each
+    "step" is a bounded sample of the workload from which a full step's time
+    is extrapolated; the line says so (`extrapolated`, `samples_timed`)."""
     if rank != 0:
         return None
     import oracle
     oracle.build()
     ests = []
     sample = ""
+    n_timed = 0
+    t0 = time.perf_counter()
     for i in range(args.warmup + args.steps):
-        est, sample = oracle_step_estimate(budget_s=args.cpu_budget / 3)
+        est, sample, k = oracle_step_estimate(budget_s=args.cpu_budget / 3)
         if i >= args.warmup:
             ests.append(est)
+            n_timed += k
+    wall = time.perf_counter() - t0
     s_step = statistics.median(ests)
     value = N_GEMMS * GEMM_FLOPS / s_step / 1e12
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32 decisions, f64 GEMM accumulation (oracle)",
             "data": "synthetic", "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "extrapolated": True,
+            "extrapolation": (f"each of the {args.steps} timed steps is {n_timed // max(args.steps, 1)} bounded "
+                              f"oracle samples (about {args.cpu_budget / 3:.0f} s of CPU work) whose per-element "
+                              f"and per-MAC times are scaled to one full step; ms_per_step is that estimate, "
+                              f"not a measured step ({wall:.1f} s of wall time in all)"),
+            "samples_timed": n_timed,
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample,
+                             "host_nproc": host_cores()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------- one kernel, for ncu ----
+
+def run_case(argv):
+    """One library kernel on synthetic device data, for profiler captures:
+
+      --case gemm M N K [f32]      random codes, E4M3 scales in [2^-6, 2^2)
+      --case quantize ROWS COLS rn|sr
+      --case quantize_2d ROWS COLS
+      --case rht T C rn|sr
+      --case dual T C rn|sr
+      --case noise ROWS COLS
+
+    Two warm-up launches, then --steps launches; prints the mean CUDA-event
+    time per launch (not a benchmark while a profiler is attached)."""
+    import torch
+
+    import nvfp4_bit_quantized_quantize_gb300 as nv
+    from __graft_entry__ import build
+
+    build()
+    kind, rest = argv[0], argv[1:]
+    reps = CASE_REPS[0]
+    torch.manual_seed(0)
+    ws = nv.alloc_workspace()
+    if kind == "gemm":
+        M, N, K = (int(v) for v in rest[:3])
+        f32 = len(rest) > 3 and rest[3] == "f32"
+        a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device="cuda")
+        b = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda")
+        sfa = torch.randint(0x18, 0x48, (nv.nvfp4_sf_bytes(M, K),), dtype=torch.uint8, device="cuda")
+        sfb = torch.randint(0x18, 0x48, (nv.nvfp4_sf_bytes(N, K),), dtype=torch.uint8, device="cuda")
+        one = torch.ones(1, device="cuda")
+        d = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device="cuda")
+        fn = lambda: nv.nvfp4_gemm(a, sfa, one, b, sfb, one, M, N, K, d, N, nv.OUT_F32 if f32 else nv.OUT_BF16,
+                                   ws)
+        what = f"gemm {M}x{N}x{K}{' f32' if f32 else ''}"
+        work = lambda ms: f"{2 * M * N * K / ms / 1e9:.1f} TFLOP/s"
+    else:
+        R, C = int(rest[0]), int(rest[1])
+        mode = nv.SR if (len(rest) > 2 and rest[2] == "sr") else nv.RN
+        x = torch.randn((R, C), dtype=torch.bfloat16, device="cuda")
+        if kind == "quantize":
+            q, sf, g = nv.alloc_quantized(R, C)
+            fn = lambda: nv.nvfp4_quantize(x, R, C, C, mode, 1, q, sf, g, ws)
+        elif kind == "quantize_2d":
+            q, sf, g = nv.alloc_quantized(R, C)
+            qT, sfT, _ = nv.alloc_quantized(C, R)
+            fn = lambda: nv.nvfp4_quantize_2d(x, R, C, C, q, sf, qT, sfT, g, ws)
+        elif kind == "rht":
+            q, sf, g = nv.alloc_quantized(C, R)
+            fn = lambda: nv.nvfp4_rht_quantize(x, R, C, C, 5, mode, 1, q, sf, g, ws)
+        elif kind == "dual":
+            q, sf, g = nv.alloc_quantized(R, C)
+            qT, sfT, gT = nv.alloc_quantized(C, R)
+            fn = lambda: nv.nvfp4_quantize_dual(x, R, C, C, mode, 1, q, sf, g, 5, mode, 2, qT, sfT, gT, ws)
+        elif kind == "noise":
+            q, sf, g = nv.alloc_quantized(R, C)
+            nv.nvfp4_quantize(x, R, C, C, nv.RN, 0, q, sf, g, ws)
+            sums = torch.empty(2, dtype=torch.float64, device="cuda")
+            fn = lambda: nv.nvfp4_quant_noise(x, R, C, C, q, sf, g, sums)
+        else:
+            raise SystemExit(run_case.__doc__)
+        what = f"{kind} {R}x{C}{' sr' if mode == nv.SR else ''}"
+        byts = 2.5625 * R * C if kind == "noise" else quant_bytes(
+            {"quantize": "quantize_1x16", "quantize_2d": "quantize_2d_t", "rht": "rht_quantize",
+             "dual": "quantize_dual"}[kind], R, C)
+        work = lambda ms: f"{byts / ms / 1e6:.1f} GB/s algorithmic"
+    stream = torch.cuda.current_stream()
+    ms = _event_ms(fn, stream, reps=reps, warmup=2)
+    st = nv.nvfp4_device_status(ws)
+    if st != 0:
+        raise SystemExit(f"device status {nv.nvfp4_status_str(st)}")
+    print(f"{what}: {ms:.4f} ms per launch, {work(ms)}")
+
+
+CASE_REPS = [3]
 
 
 def main():
@@ -723,7 +862,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--case", nargs="+", metavar="ARG",
+                    help="run one kernel for a profiler capture instead of the benchmark "
+                         "(gemm M N K [f32] | quantize R C rn|sr | quantize_2d R C | rht T C rn|sr | "
+                         "dual T C rn|sr | noise R C); --steps launches after 2 warm-up launches")
     args = ap.parse_args()
+    if args.case:
+        CASE_REPS[0] = args.steps
+        run_case(args.case)
+        return
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
 

@@ -77,7 +77,7 @@ typedef enum {
     NVFP4_ERR_NONFINITE = 4,   /* input holds Inf or NaN (device-detected) */
     NVFP4_ERR_TIMEOUT = 5,     /* a bounded device wait ran out (device-detected) */
     NVFP4_ERR_CUDA = 6,        /* a CUDA runtime or driver call failed */
-    NVFP4_ERR_UNSUPPORTED = 7  /* device is not sm_103 / sm_100 family */
+    NVFP4_ERR_UNSUPPORTED = 7  /* device is not sm_103 (the library carries sm_103a code only) */
 } nvfp4_status;
 
 typedef enum { NVFP4_ROUND_RN = 0, NVFP4_ROUND_SR = 1 } nvfp4_round;
@@ -285,11 +285,19 @@ nvfp4_status nvfp4_encode_probe(const float* v, const uint16_t* r, int64_t n,
  *  - each call clears the scratch on `stream` before its launch; all calls
  *    share the one array, so calls that overlap on the GPU (e.g. on two
  *    streams at once) race — serialise them, e.g. on one stream;
- *  - the first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture begins;
- *  - device-detected errors are not kept anywhere the caller can query; a
- *    non-finite input shows up as a non-finite *g_dec.
+ *  - every call looks up the array's device address (cudaGetSymbolAddress,
+ *    which allocates nothing) with the calling thread's device current, so an
+ *    address that moved after cudaDeviceReset or a module reload is never
+ *    reused; while `stream` is capturing, the address looked up by the last
+ *    call on that device outside a capture is used, so make the first call on
+ *    each device before any stream capture begins;
+ *  - device-detected errors are not kept anywhere the caller can query, and
+ *    the next call's clear erases them: a non-finite input shows up as a
+ *    non-finite *g_dec, but a bounded device wait that runs out (the grid
+ *    barrier after 2 s, NVFP4_ERR_TIMEOUT under nvfp4_quantize) leaves finite,
+ *    wrong codes, scales and *g_dec that nothing reports.  Callers that need
+ *    to see those errors use nvfp4_quantize with a workspace and
+ *    nvfp4_device_status.
  */
 nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                     nvfp4_round mode, uint64_t sr_seed,

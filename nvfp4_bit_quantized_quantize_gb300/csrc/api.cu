@@ -105,6 +105,24 @@ nvfp4_status launch_encode_probe(const float* v, const uint16_t* r, int64_t n, u
     return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+// 128-row x 64-column tiles, 1x16 blocks along the rows.
+QuantParams params_1x16(int64_t rows, int64_t cols, int mode, uint64_t sr_seed, uint8_t* q, uint8_t* sf,
+                        float* g_dec)
+{
+    QuantParams p = {};
+    p.rows = rows;
+    p.cols = cols;
+    p.tiles_c = (cols + 63) / 64;
+    p.tiles_r = (rows + 127) / 128;
+    p.ntiles = p.tiles_r * p.tiles_c;
+    p.q = q;
+    p.sf = sf;
+    p.g_dec = g_dec;
+    p.sr_seed = sr_seed;
+    p.mode = mode;
+    return p;
+}
+
 }  // namespace nvfp4
 
 // ------------------------------------------------------------------ C ABI ----
@@ -182,17 +200,7 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
     nvfp4_status st = check_device();
     if (st != NVFP4_OK)
         return st;
-    QuantParams p = {};
-    p.rows = rows;
-    p.cols = cols;
-    p.tiles_c = cdiv(cols, 64);
-    p.tiles_r = cdiv(rows, 128);
-    p.ntiles = p.tiles_r * p.tiles_c;
-    p.q = q;
-    p.sf = sf;
-    p.g_dec = g_dec;
-    p.sr_seed = sr_seed;
-    p.mode = mode;
+    const QuantParams p = params_1x16(rows, cols, mode, sr_seed, q, sf, g_dec);
     return launch_quantize(QuantKind::k1x16, x, ld, p, static_cast<Workspace*>(ws), (cudaStream_t)stream);
 }
 

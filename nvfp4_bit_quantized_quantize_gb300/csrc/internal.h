@@ -47,6 +47,11 @@ struct QuantParams {
 
 enum class QuantKind { k1x16, k2d, kRht, kDual };
 
+// Launch parameters of the 1x16 quantizer (nvfp4_quantize and its
+// allocation-free variant build them here, so the two cannot drift apart).
+QuantParams params_1x16(int64_t rows, int64_t cols, int mode, uint64_t sr_seed, uint8_t* q, uint8_t* sf,
+                        float* g_dec);
+
 // Host launchers (quantize.cu, gemm.cu, noise.cu, mxfp4.cu, probe.cu).  They assume the
 // arguments were validated by the C-ABI layer.
 nvfp4_status launch_quantize(QuantKind kind, const void* x, int64_t ld, const QuantParams& p, Workspace* ws,

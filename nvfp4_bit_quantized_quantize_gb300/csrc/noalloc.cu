@@ -30,19 +30,28 @@ static_assert(kNoAllocScratchBytes >= sizeof(Workspace), "scratch holds one work
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch per device, looked up on the first call
-// made with that device current.  (In host code the symbol is only a host-side
-// stand-in; only cudaGetSymbolAddress yields the device address.)
+// Device address of g_noalloc_scratch for the current device.  In host code
+// the symbol is only a host-side stand-in; cudaGetSymbolAddress, with the
+// device current, yields the device address.  It is looked up on every call
+// that is not being captured (it allocates nothing and costs little), so an
+// address that changed after cudaDeviceReset or a module reload is never
+// reused; a call on a capturing stream takes the address the last uncaptured
+// call on that device found.
 std::mutex g_setup_mutex;
 void* g_scratch_ptr[64] = {};
 
-nvfp4_status scratch_for_current_device(void** out)
+nvfp4_status scratch_for_current_device(cudaStream_t stream, void** out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return NVFP4_ERR_CUDA;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();  // an unqueryable stream is treated as not capturing
+        cs = cudaStreamCaptureStatusNone;
+    }
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (cs == cudaStreamCaptureStatusNone || g_scratch_ptr[dev] == nullptr) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
             return NVFP4_ERR_CUDA;
@@ -53,7 +62,6 @@ nvfp4_status scratch_for_current_device(void** out)
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
@@ -78,22 +86,13 @@ extern "C" nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int6
         return NVFP4_ERR_UNSUPPORTED;
 
     void* scratch = nullptr;
-    nvfp4_status st = scratch_for_current_device(&scratch);
+    nvfp4_status st = scratch_for_current_device((cudaStream_t)stream, &scratch);
     if (st != NVFP4_OK)
         return st;
     // the barrier counters, amax and status must start at zero
     if (cudaMemsetAsync(scratch, 0, kNoAllocScratchBytes, (cudaStream_t)stream) != cudaSuccess)
         return NVFP4_ERR_CUDA;
 
-    QuantParams p = {};
-    p.rows = rows;
-    p.cols = cols;
-    p.tiles_c = cdiv(cols, 64);
-    p.ntiles = cdiv(rows, 128) * p.tiles_c;
-    p.q = q;
-    p.sf = sf;
-    p.g_dec = g_dec;
-    p.sr_seed = sr_seed;
-    p.mode = mode;
+    const QuantParams p = params_1x16(rows, cols, mode, sr_seed, q, sf, g_dec);
     return launch_quantize(QuantKind::k1x16, x, ld, p, static_cast<Workspace*>(scratch), (cudaStream_t)stream);
 }
