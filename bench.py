@@ -190,7 +190,19 @@ def run_e2e(step, args, stream):
     """K steps through the public API with host buffers: every step copies its
     inputs from pinned host memory and its results back.  Copies run on their
     own streams into/out of two device slots, so step k's compute overlaps the
-    input copy of step k+1 and the result copy of step k-1."""
+    input copy of step k+1 and the result copy of step k-1.  `args.warmup`
+    untimed steps of the same pipeline run first (the first copies through
+    fresh streams and buffers are slow)."""
+    import torch
+
+    if getattr(args, "warmup", 0) > 0:
+        import types
+        _e2e_steps(step, types.SimpleNamespace(steps=args.warmup), stream)
+        torch.cuda.synchronize(step.dev)
+    return _e2e_steps(step, args, stream)
+
+
+def _e2e_steps(step, args, stream):
     import torch
 
     dev = step.dev

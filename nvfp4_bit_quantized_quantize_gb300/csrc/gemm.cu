@@ -9,8 +9,15 @@
 // padded on chip: tensor loads past the edges read zeros, the scale buffers'
 // padding (zero, as the quantizers write it) covers the last atoms, and
 // output chunks that cross M or N are written with plain stores of the
-// elements inside M x N.  Each CTA owns a persistent sequence of 128 x 256
-// output tiles:
+// elements inside M x N.
+//
+// Two kernels: the paired-SM kernel at the end of this file (256 x 256 tiles
+// on two SMs, tcgen05 cta_group::2) runs every matrix of more than 128 rows;
+// the one-SM kernel here (128 x 256 tiles) runs the rest.  Both are bound by
+// shared-memory traffic per SM (tensor-copy writes, tensor-core operand
+// reads, the scale warps' reads, epilogue staging); the pair moves a third
+// less of it per flop.  In the one-SM kernel each CTA owns a persistent
+// sequence of 128 x 256 output tiles:
 //   warp 0  TMA producer: A/B tiles (128-byte swizzle) and the scale atoms
 //           (3-D tensor boxes of 4 atoms) into a 4-stage shared-memory ring;
 //   warp 1  allocates tensor memory and issues tcgen05.mma.kind::mxf4nvf4
@@ -334,18 +341,330 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ============================================================ paired SMs ====
+// The same GEMM on two SMs per output tile (tcgen05 cta_group::2): a cluster
+// of two CTAs computes a 256 x 256 tile with one M = 256, N = 256, K = 64 MMA
+// per step, issued by one thread of the even CTA.  Each CTA stages its own
+// 128 rows of A and its own 128 rows of B (the tensor cores exchange the B
+// halves), so each SM receives 38 KB per K = 256 stage (A, B and the scale
+// atoms) instead of the one-SM kernel's 54 KB for the same work, and the
+// freed shared memory holds a fifth stage.  Each CTA's tensor memory holds
+// the accumulator of its 128 A rows (256 columns) and, per stage, its A rows'
+// scale atoms and the atoms of all 256 B rows, written there by its own four
+// scale warps with tcgen05.st.
+//   warp 0     TMA producer (both CTAs): this CTA's A and B boxes, its A
+//              rows' scale atoms and both B row tiles' atoms, all on this
+//              CTA's `full` barrier;
+//   warp 1     tensor-memory allocation (collective over the pair); in the
+//              even CTA, the MMA issuer;
+//   warps 2-9  epilogue, as in the one-SM kernel;
+//   warps 10-13 scale warps: once their CTA's stage landed and the
+//              tensor-memory slot is free, tcgen05.st of the atoms, then one
+//              arrive on the even CTA's sf_ready barrier of the stage -- eight
+//              arrivals (four per CTA) say that both CTAs' stage is in place,
+//              so the MMA thread waits on that one barrier per stage.
+// Stage-free, slot-free and accumulator-full signals reach both CTAs through
+// the multicast form of tcgen05.commit; the odd CTA's scale-ready and
+// drained-accumulator signals reach the even CTA by remote mbarrier arrives
+// with the default (CTA-scope release) semantics: what they report was
+// completed by an earlier wait of the arriving thread (TMA completion,
+// tcgen05.wait::st or ::ld, then tcgen05.fence::before_thread_sync), and a
+// cluster-scope release on these arrives halved the kernel's speed.  Every
+// wait is bounded; a cluster barrier keeps both CTAs (whose shared and tensor
+// memory the MMAs use) alive until all tensor-core work is done.
+constexpr int PM = 256;
+constexpr int PN = 256;
+constexpr int kPA = 128 * BK / 2;              // 16 KB: this CTA's 128 rows of A
+constexpr int kPB = 128 * BK / 2;              // 16 KB: this CTA's 128 rows of B
+constexpr int kPStage = kPA + kPB + kSfaBytes + kSfbBytes;
+constexpr int kPStages = 5;                    // shared-memory ring (5 x 38 KB)
+constexpr int kPSlots = 4;                     // scale slots in tensor memory (a ring of their own)
+constexpr uint32_t kPSlotStride = 64;          // A's 4 steps x 4 columns, B's 4 steps x 8 (48 used)
+
+struct PairCtl {
+    uint64_t full[kPStages];      // this CTA's stage landed
+    uint64_t empty[kPStages];     // the stage's MMAs are done (multicast commit)
+    uint64_t sf_ready[kPStages];  // even CTA: both CTAs' stage landed and its scales are in tensor memory
+    uint64_t sf_free[kPSlots];    // the MMAs reading the scale slot are done (multicast commit)
+    uint64_t tmem_full;
+    uint64_t tmem_empty;          // even CTA: both CTAs drained the accumulator (16 arrivals)
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kPSmemBytes = 1024 + (size_t)kPStages * kPStage + kEpilogueWarps * kStoreBufBytes + sizeof(PairCtl);
+static_assert(kPStage % 1024 == 0, "stage alignment");
+static_assert(kAccCols + kPSlots * kPSlotStride <= kTmemCols, "tensor memory budget");
+static_assert(kPSmemBytes <= 227 * 1024, "shared memory budget");
+
+constexpr uint32_t kIdescNvf4Pair = mma_idesc<false>(PM, PN);
+constexpr uint32_t kIdescMxf4Pair = mma_idesc<true>(PM, PN);
+
+template <bool kMx>
+__device__ __forceinline__ void mma_step_pair(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t sfa, uint32_t sfb,
+                                              uint32_t acc)
+{
+    if constexpr (kMx)
+        mma_mxf4_pair(d, adesc, bdesc, kIdescMxf4Pair, sfa, sfb, acc);
+    else
+        mma_nvf4_pair(d, adesc, bdesc, kIdescNvf4Pair, sfa, sfb, acc);
+}
+
+template <bool kMx>
+__global__ void __launch_bounds__(kThreads, 1)
+    nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                          const __grid_constant__ CUtensorMap tma_sfa, const __grid_constant__ CUtensorMap tma_sfb,
+                          const __grid_constant__ CUtensorMap tma_d, const GemmArgs args, Workspace* ws)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* store_buf = smem + (size_t)kPStages * kPStage;
+    PairCtl* ctl = reinterpret_cast<PairCtl*>(store_buf + kEpilogueWarps * kStoreBufBytes);
+    volatile int* abort = &ctl->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the MMAs
+    const uint32_t cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const uint32_t tiles_m = ((uint32_t)args.M + PM - 1) / PM;
+    const uint32_t tiles_n = ((uint32_t)args.N + PN - 1) / PN;
+    const uint32_t ntiles = tiles_m * tiles_n;
+    const uint32_t kstages = ((uint32_t)args.K + BK - 1) / BK;
+    // this cluster's tiles are cluster, cluster + nclusters, ...; iteration i
+    // of every role is K stage i % kstages of its (i / kstages)-th tile
+    const uint32_t my_tiles = (ntiles - cluster + nclusters - 1) / nclusters;
+    const uint32_t iters = my_tiles * kstages;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->sf_ready[s], 2 * kScaleWarps);
+        }
+        for (int s = 0; s < kPSlots; ++s)
+            mbar_init(&ctl->sf_free[s], 1);
+        mbar_init(&ctl->tmem_full, 1);
+        mbar_init(&ctl->tmem_empty, 2 * kEpilogueWarps);
+        mbar_init(&ctl->drain, 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+        tc_fence_before();
+    }
+    __syncthreads();
+    // both CTAs' barriers are initialised before any remote arrive
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------- TMA producer ----
+        tma_prefetch_desc(&tma_a);
+        tma_prefetch_desc(&tma_b);
+        tma_prefetch_desc(&tma_sfa);
+        tma_prefetch_desc(&tma_sfb);
+        uint32_t ia = 0;  // stages issued
+        for (; ia < iters && !*abort; ++ia) {
+            const uint32_t s = ia % kPStages;
+            if (ia >= kPStages && !mbar_wait(&ctl->empty[s], ((ia / kPStages) - 1) & 1, ws, abort))
+                break;
+            const uint32_t t = cluster + (ia / kstages) * nclusters, ks = ia % kstages;
+            const uint32_t tm = t % tiles_m, tn = t / tiles_m;
+            const uint32_t arow = 2 * tm + rank;   // this CTA's 128-row tile of A
+            uint8_t* st = smem + (size_t)s * kPStage;
+            // boxes past M, N or K read as zeros and still count in full
+            mbar_expect_tx(&ctl->full[s], kPStage);
+            tma_load_2d(st, &tma_a, &ctl->full[s], (int32_t)(ks * 128), (int32_t)(arow * 128));
+            tma_load_2d(st + kPA, &tma_b, &ctl->full[s], (int32_t)(ks * 128), (int32_t)((2 * tn + rank) * 128));
+            tma_load_3d(st + kPA + kPB, &tma_sfa, &ctl->full[s], 0, (int32_t)(ks * 4), (int32_t)arow);
+            tma_load_3d(st + kPA + kPB + kSfaBytes, &tma_sfb, &ctl->full[s], 0, (int32_t)(ks * 4),
+                        (int32_t)(2 * tn));
+        }
+        // never leave with copies in flight
+        for (uint32_t k = ia > kPStages ? ia - kPStages : 0; k < ia; ++k)
+            mbar_wait(&ctl->full[k % kPStages], (k / kPStages) & 1, ws, nullptr);
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ------------------------------------------------------ MMA issuer ----
+        const uint32_t base = smem_u32(smem);
+        const uint64_t a_desc = smem_desc(base, 16, 1024, kSwizzle128B);
+        const uint64_t b_desc = smem_desc(base + kPA, 16, 1024, kSwizzle128B);
+        constexpr uint32_t kStageDesc = kPStage >> 4;  // stage stride in descriptor units
+        constexpr uint16_t kBoth = 0x3;
+        uint32_t i = 0;
+        for (uint32_t n = 0; n < my_tiles && !*abort; ++n) {
+            if (n > 0 && !mbar_wait(&ctl->tmem_empty, (n - 1) & 1, ws, abort))
+                break;
+            tc_fence_after();
+            for (uint32_t ks = 0; ks < kstages; ++ks, ++i) {
+                const uint32_t s = i % kPStages, u = i % kPSlots;
+                // both CTAs' scale warps saw their stage land and wrote its
+                // scale atoms before they signalled
+                if (!mbar_wait(&ctl->sf_ready[s], (i / kPStages) & 1, ws, abort))
+                    goto mma_done;
+                tc_fence_after();
+                const uint64_t off = (uint64_t)(s * kStageDesc);
+                const uint32_t sfa_t = tmem + kAccCols + u * kPSlotStride;
+                const uint32_t sfb_t = sfa_t + 16;
+                const uint32_t k_left = (uint32_t)args.K - ks * BK;
+                if (k_left >= BK) {
+#pragma unroll
+                    for (uint32_t j = 0; j < 4; ++j)
+                        mma_step_pair<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
+                                           sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                } else {
+                    const uint32_t kk = (k_left + 63) / 64;
+                    for (uint32_t j = 0; j < kk; ++j)
+                        mma_step_pair<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
+                                           sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                }
+                tc_commit_pair_multicast(&ctl->empty[s], kBoth);
+                tc_commit_pair_multicast(&ctl->sf_free[u], kBoth);
+            }
+            tc_commit_pair_multicast(&ctl->tmem_full, kBoth);
+        }
+    mma_done:
+        // all tensor-core work issued by this thread completes before teardown
+        tc_commit_pair_multicast(&ctl->drain, 0x1);
+        mbar_wait(&ctl->drain, 0, ws, nullptr);
+    } else if (warp >= 2 && warp < kFirstScaleWarp) {
+        // -------------------------------------------------------- epilogue ----
+        const uint32_t q = warp & 3;             // tensor-memory lane quarter of this warp
+        const uint32_t half = (warp - 2) >> 2;   // columns 128*half .. +127
+        const float alpha = kMx ? 1.0f : __fmul_rn(*args.ga, *args.gb);
+        const uint32_t empty_addr = mapa_shared(smem_u32(&ctl->tmem_empty), 0);
+        for (uint32_t n = 0; n < my_tiles && !*abort; ++n) {
+            const uint32_t t = cluster + n * nclusters;
+            const uint32_t tm = t % tiles_m, tn = t / tiles_m;
+            if (!mbar_wait(&ctl->tmem_full, n & 1, ws, abort))
+                break;
+            tc_fence_after();
+            const int32_t c0 = (int32_t)(tn * PN + half * 128);
+            const int32_t row0 = (int32_t)(tm * PM + rank * 128 + q * 32);
+            const bool live = c0 < args.N && row0 < args.M;
+            uint8_t* buf = store_buf + (warp - 2) * kStoreBufBytes;
+            const uint32_t taddr = tmem + ((q * 32) << 16) + half * 128;
+            if (args.out_f32) {
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + h * 32, r);
+                    tmem_ld_wait();
+                    if (live)
+                        epilogue_store_f32(r, alpha, row0, c0 + h * 32, args, buf, &tma_d, lane);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_remote(empty_addr);
+            } else {
+                uint32_t p[64];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld_32x32b_x32(taddr + h * 64, ra);
+                    tmem_ld_32x32b_x32(taddr + h * 64 + 32, rb);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        p[h * 32 + e] = pack_bf16x2(__fmul_rn(__uint_as_float(ra[2 * e]), alpha),
+                                                    __fmul_rn(__uint_as_float(ra[2 * e + 1]), alpha));
+                        p[h * 32 + 16 + e] = pack_bf16x2(__fmul_rn(__uint_as_float(rb[2 * e]), alpha),
+                                                         __fmul_rn(__uint_as_float(rb[2 * e + 1]), alpha));
+                    }
+                }
+                // this CTA's accumulator is free once every load has landed
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_remote(empty_addr);
+                if (live)
+                    epilogue_store_bf16(p, row0, c0, args, buf, &tma_d, lane);
+            }
+        }
+        if (lane == 0)
+            bulk_wait_all();
+    } else if (warp >= kFirstScaleWarp) {
+        // ----------------------------------------------------- scale warps ----
+        // The one-SM kernel's layout: lane i takes row i (16 bytes) of every
+        // atom of the stage -- this CTA's A rows (steps 0..3), then B's row
+        // tiles 0 and 1 (steps 0..3 each) -- and writes it into its quarter's
+        // lanes: columns slot + 4j for A's step j, slot + 16 + 8j for B's.
+        const uint32_t q = warp & 3;
+        const uint32_t lanes = (q * 32) << 16;
+        const uint32_t ready0 = mapa_shared(smem_u32(&ctl->sf_ready[0]), 0);
+        for (uint32_t i = 0; i < iters; ++i) {
+            const uint32_t s = i % kPStages, u = i % kPSlots;
+            int ok = 1;
+            if (lane == 0) {
+                ok = mbar_wait(&ctl->full[s], (i / kPStages) & 1, ws, abort);
+                // the slot's previous MMAs are done
+                if (ok && i >= kPSlots)
+                    ok = mbar_wait(&ctl->sf_free[u], ((i / kPSlots) - 1) & 1, ws, abort);
+            }
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0))
+                break;
+            const uint8_t* sfa_s = smem + (size_t)s * kPStage + kPA + kPB + lane * 16;
+            const uint8_t* sfb_s = sfa_s + kSfaBytes;
+            uint32_t v[48];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 a = *reinterpret_cast<const uint4*>(sfa_s + j * 512);
+                const uint4 b0 = *reinterpret_cast<const uint4*>(sfb_s + j * 512);
+                const uint4 b1 = *reinterpret_cast<const uint4*>(sfb_s + (4 + j) * 512);
+                v[4 * j] = a.x;
+                v[4 * j + 1] = a.y;
+                v[4 * j + 2] = a.z;
+                v[4 * j + 3] = a.w;
+                v[16 + 8 * j] = b0.x;
+                v[16 + 8 * j + 1] = b0.y;
+                v[16 + 8 * j + 2] = b0.z;
+                v[16 + 8 * j + 3] = b0.w;
+                v[16 + 8 * j + 4] = b1.x;
+                v[16 + 8 * j + 5] = b1.y;
+                v[16 + 8 * j + 6] = b1.z;
+                v[16 + 8 * j + 7] = b1.w;
+            }
+            const uint32_t col = tmem + lanes + kAccCols + u * kPSlotStride;
+            tmem_st_32x32b_x16(col, v);
+            tmem_st_32x32b_x16(col + 16, v + 16);
+            tmem_st_32x32b_x16(col + 32, v + 32);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_remote(ready0 + s * (uint32_t)sizeof(uint64_t));
+        }
+    }
+
+    __syncthreads();
+    // the even CTA's MMAs read this CTA's shared memory and write its tensor
+    // memory: neither CTA frees anything before both are done
+    cluster_sync_all();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
 }  // namespace
 
 nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
                          const uint8_t* sfb, const float* gb, int64_t M, int64_t N, int64_t K, void* d,
                          int64_t ldd, nvfp4_out_dtype dt, bool mx, Workspace* ws, cudaStream_t stream)
 {
+    // 256-row pair tiles; a matrix of at most 128 rows would leave one SM of
+    // every pair without A rows, so it runs on the one-SM kernel
+    const bool pair = M > 128;
     CUtensorMap ma, mb;
     if (!encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(K / 2),
                               (uint64_t)M, (uint64_t)(K / 2), 128u, (uint32_t)BM, CU_TENSOR_MAP_SWIZZLE_128B))
         return NVFP4_ERR_CUDA;
     if (!encode_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(b), (uint64_t)(K / 2),
-                              (uint64_t)N, (uint64_t)(K / 2), 128u, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                              (uint64_t)N, (uint64_t)(K / 2), 128u, pair ? 128u : (uint32_t)BN,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
         return NVFP4_ERR_CUDA;
 
     CUtensorMap md;
@@ -358,12 +677,48 @@ nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, 
     CUtensorMap msfa, msfb;
     if (!encode_sf_atom_map(&msfa, sfa, M, K, 1) || !encode_sf_atom_map(&msfb, sfb, N, K, 2))
         return NVFP4_ERR_CUDA;
-    static bool attr_set[2][64] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return NVFP4_ERR_CUDA;
+
+    if (pair) {
+        static bool attr_set[2][64] = {};
+        static int max_clusters[2][64] = {};
+        const void* kern = mx ? (const void*)nvf4_gemm_pair_kernel<true> : (const void*)nvf4_gemm_pair_kernel<false>;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kPSmemBytes;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (!attr_set[mx][dev]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes) !=
+                cudaSuccess)
+                return NVFP4_ERR_CUDA;
+            cfg.gridDim = dim3(2, 1, 1);
+            int mc = 0;
+            if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess || mc < 1)
+                return NVFP4_ERR_CUDA;
+            max_clusters[mx][dev] = mc;
+            attr_set[mx][dev] = true;
+        }
+        const int64_t ntiles = ((M + PM - 1) / PM) * ((N + PN - 1) / PN);
+        const int64_t clusters = ntiles < max_clusters[mx][dev] ? ntiles : max_clusters[mx][dev];
+        cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+        const cudaError_t e =
+            mx ? cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<true>, ma, mb, msfa, msfb, md, args, ws)
+               : cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<false>, ma, mb, msfa, msfb, md, args, ws);
+        return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+    }
+
+    static bool attr_set[2][64] = {};
     const void* kern = mx ? (const void*)nvf4_gemm_kernel<true> : (const void*)nvf4_gemm_kernel<false>;
-    if (dev < 64 && !attr_set[mx][dev]) {
+    if (!attr_set[mx][dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
             return NVFP4_ERR_CUDA;
         attr_set[mx][dev] = true;

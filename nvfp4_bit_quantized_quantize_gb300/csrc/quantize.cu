@@ -55,16 +55,6 @@ constexpr size_t kSmemBytes = 1024 + (size_t)kMaxStages * kTileBytes + sizeof(Sm
 // rows are 128 bytes.
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
 
-// Tile index -> (index along the strided axis, index along the contiguous
-// axis) in 32-bit arithmetic (tile counts stay far below 2^32).
-__device__ __forceinline__ void tile_coords(int64_t t, const QuantParams& p, int64_t& major, int64_t& minor)
-{
-    const uint32_t tt = (uint32_t)t, tc = (uint32_t)p.tiles_c;
-    const uint32_t q = tt / tc;
-    major = q;
-    minor = tt - q * tc;
-}
-
 // --------------------------------------------------------- block quantize ----
 // Scale and round one block of 16 binary32 values.  Returns the scale byte;
 // writes 8 bytes of packed codes.  ftab holds rn(s_enc / E4M3value(b)) for the
@@ -139,6 +129,17 @@ __device__ __forceinline__ void tensor_scales(float amax, float& s_enc, float& g
     g = __fdiv_rn(amax, 2688.0f);
 }
 
+// max |.| over the 16 bf16 values of two 16-byte loads, as a tree of depth 3
+// (NaN-propagating bf16x2 accumulator, as hmax_to_float reads it).
+__device__ __forceinline__ uint32_t habs_max16(const uint4& a, const uint4& b)
+{
+    const uint32_t m0 = habs_max2(habs_max2(0u, a.x), a.y);
+    const uint32_t m1 = habs_max2(habs_max2(0u, a.z), a.w);
+    const uint32_t m2 = habs_max2(habs_max2(0u, b.x), b.y);
+    const uint32_t m3 = habs_max2(habs_max2(0u, b.z), b.w);
+    return habs_max2(habs_max2(m0, m1), habs_max2(m2, m3));
+}
+
 // Scan a 128 x 64 bf16 tile for max |x| (bf16x2 accumulator, NaN-propagating):
 // thread ctid reads block (row ctid / 4, block ctid % 4).
 __device__ __forceinline__ uint32_t scan_tile_bf16(const uint8_t* tile, int ctid)
@@ -146,27 +147,17 @@ __device__ __forceinline__ uint32_t scan_tile_bf16(const uint8_t* tile, int ctid
     const uint32_t row = (uint32_t)ctid >> 2, blk = ctid & 3;
     const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
     const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
-    uint32_t acc = habs_max2(0u, a.x);
-    acc = habs_max2(acc, a.y);
-    acc = habs_max2(acc, a.z);
-    acc = habs_max2(acc, a.w);
-    acc = habs_max2(acc, b.x);
-    acc = habs_max2(acc, b.y);
-    acc = habs_max2(acc, b.z);
-    acc = habs_max2(acc, b.w);
-    return acc;
+    return habs_max16(a, b);
 }
 
 // ------------------------------------------------------------------ 1x16 ----
 // Consumer thread ctid owns block (row ctid / 4, block ctid % 4) of the tile;
 // the 4 blocks of a row sit in lanes 4i..4i+3 of one warp.
 struct Op1x16 {
-    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
-                                 const QuantParams& p)
+    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tr, int32_t tc,
+                                 const QuantParams&)
     {
-        int64_t tr, tc;
-        tile_coords(tile, p, tr, tc);
-        tma_load_2d(dst, m, bar, (int32_t)(tc * 64), (int32_t)(tr * 128));
+        tma_load_2d(dst, m, bar, tc * 64, tr * 128);
     }
 
     __device__ static uint2 phase1(const uint8_t* tile, int ctid, const QuantParams&)
@@ -174,26 +165,23 @@ struct Op1x16 {
         return make_uint2(__float_as_uint(hmax_to_float(scan_tile_bf16(tile, ctid))), 0u);
     }
 
-    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, const float (&s_enc)[2],
+    __device__ static void phase2(const uint8_t* tile, int32_t tr, int32_t tc, int ctid, const float (&s_enc)[2],
                                   const float (*ftab)[128], const QuantParams& p)
     {
-        int64_t tr, tc;
-        tile_coords(t, p, tr, tc);
         const int lane = ctid & 31;
         const uint32_t row = (uint32_t)ctid >> 2, blk = ctid & 3;
         const uint4 a = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk));
         const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         float x[16];
-        uint32_t acc = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             x[2 * j] = bf16lo(w[j]);
             x[2 * j + 1] = bf16hi(w[j]);
-            acc = habs_max2(acc, w[j]);
         }
-        const int64_t grow = tr * 128 + row;
-        const int64_t gcol = tc * 64 + blk * 16;
+        const uint32_t acc = habs_max16(a, b);
+        const int64_t grow = (int64_t)tr * 128 + row;
+        const int64_t gcol = (int64_t)tc * 64 + blk * 16;
         uint32_t lo32, hi32;
         const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc[0], ftab[0], p.mode, p.sr_seed,
                                           (uint64_t)(grow * (p.cols / 16) + gcol / 16), lo32, hi32);
@@ -203,7 +191,7 @@ struct Op1x16 {
         const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
         const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
         if ((lane & 3) == 0) {
-            const int64_t atom = (tr * p.tiles_c + tc) * 512;
+            const int64_t atom = ((int64_t)tr * p.tiles_c + tc) * 512;
             *reinterpret_cast<uint32_t*>(p.sf + atom + (row & 31) * 16 + (row >> 5) * 4) =
                 sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
         }
@@ -234,10 +222,10 @@ __device__ __forceinline__ uint64_t nibble_transpose16(uint64_t w, int i)
 // Each half-warp owns one 16 x 16 tile: lanes 0-15 tile 2w, lanes 16-31 tile
 // 2w + 1 of the 32 tiles (8 row groups x 4 column blocks); lane i has row i.
 struct Op2d {
-    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
+    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tr, int32_t tc,
                                  const QuantParams& p)
     {
-        Op1x16::issue(m, dst, bar, tile, p);
+        Op1x16::issue(m, dst, bar, tr, tc, p);
     }
 
     __device__ static uint2 phase1(const uint8_t* tile, int ctid, const QuantParams& p)
@@ -245,11 +233,9 @@ struct Op2d {
         return Op1x16::phase1(tile, ctid, p);
     }
 
-    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, const float (&s_enc)[2],
+    __device__ static void phase2(const uint8_t* tile, int32_t tr, int32_t tc, int ctid, const float (&s_enc)[2],
                                   const float (*ftab)[128], const QuantParams& p)
     {
-        int64_t tr, tc;
-        tile_coords(t, p, tr, tc);
         const int lane = ctid & 31, cw = ctid >> 5;
         const int64_t kblocksT = p.rows / 16;
         const int64_t cpT = (kblocksT + 3) / 4;
@@ -260,28 +246,27 @@ struct Op2d {
         const uint4 b = *reinterpret_cast<const uint4*>(tile + sw128(row, 2 * blk + 1));
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         float x[16];
-        uint32_t acc = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             x[2 * j] = bf16lo(w[j]);
             x[2 * j + 1] = bf16hi(w[j]);
-            acc = habs_max2(acc, w[j]);
         }
+        const uint32_t acc = habs_max16(a, b);
         uint32_t m = __float_as_uint(hmax_to_float(acc));
 #pragma unroll
         for (int off = 1; off < 16; off <<= 1)
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-        const int64_t grow = tr * 128 + row;
-        const int64_t gcol = tc * 64 + blk * 16;
+        const int64_t grow = (int64_t)tr * 128 + row;
+        const int64_t gcol = (int64_t)tc * 64 + blk * 16;
         uint32_t lo32, hi32;
         const uint32_t sb = quant_block16(x, __uint_as_float(m), s_enc[0], ftab[0], NVFP4_ROUND_RN, 0, 0, lo32, hi32);
         if (grow < p.rows && gcol < p.cols)
             *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
-        p.sf[(tr * p.tiles_c + tc) * 512 + (row & 31) * 16 + (row >> 5) * 4 + blk] = (uint8_t)sb;
+        p.sf[((int64_t)tr * p.tiles_c + tc) * 512 + (row & 31) * 16 + (row >> 5) * 4 + blk] = (uint8_t)sb;
         if (p.qT != nullptr) {
             const uint64_t col = nibble_transpose16(((uint64_t)hi32 << 32) | lo32, (int)i);
             const int64_t rT = gcol + i;     // row of the transposed matrix
-            const int64_t kbT = tr * 8 + g;  // its 16-block index
+            const int64_t kbT = (int64_t)tr * 8 + g;  // its 16-block index
             if (rT < p.cols && kbT < kblocksT)
                 *reinterpret_cast<uint2*>(p.qT + rT * (p.rows / 2) + kbT * 8) =
                     make_uint2((uint32_t)col, (uint32_t)(col >> 32));
@@ -305,13 +290,11 @@ struct Op2d {
 // warp w handles token block tb = w / 4 and channels 32 (w % 4) .. + 31, one
 // channel per lane, 16 tokens per thread.
 struct OpRht {
-    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
-                                 const QuantParams& p)
+    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tt, int32_t ct,
+                                 const QuantParams&)
     {
-        int64_t tt, ct;
-        tile_coords(tile, p, tt, ct);
-        tma_load_2d(dst, m, bar, (int32_t)(ct * 128), (int32_t)(tt * 64));
-        tma_load_2d(dst + 8192, m, bar, (int32_t)(ct * 128 + 64), (int32_t)(tt * 64));
+        tma_load_2d(dst, m, bar, ct * 128, tt * 64);
+        tma_load_2d(dst + 8192, m, bar, ct * 128 + 64, tt * 64);
     }
 
     // D v for this thread's channel and token block, as pairs P[k] =
@@ -389,11 +372,10 @@ struct OpRht {
 
     // Quantize this thread's transformed channel block into (q, sf) with the
     // given tensor scale.
-    __device__ static void quantize_out(const uint8_t* tile, int64_t t, int ctid, float s_enc, const float* ftab,
-                                        int mode, uint64_t seed, uint8_t* q, uint8_t* sf, const QuantParams& p)
+    __device__ static void quantize_out(const uint8_t* tile, int32_t tt, int32_t ct, int ctid, float s_enc,
+                                        const float* ftab, int mode, uint64_t seed, uint8_t* q, uint8_t* sf,
+                                        const QuantParams& p)
     {
-        int64_t tt, ct;
-        tile_coords(t, p, tt, ct);
         const int lane = ctid & 31, cw = ctid >> 5;
         const uint32_t tb = cw >> 2, cl = (cw & 3) * 32 + lane;
         const int64_t T = p.rows, C = p.cols;
@@ -405,20 +387,20 @@ struct OpRht {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             bamax = fmaxf(bamax, fabsf(y[i]));
-        const int64_t c = ct * 128 + cl;
-        const int64_t kb = tt * 4 + tb;
+        const int64_t c = (int64_t)ct * 128 + cl;
+        const int64_t kb = (int64_t)tt * 4 + tb;
         uint32_t lo32, hi32;
         const uint32_t sb =
             quant_block16(y, bamax, s_enc, ftab, mode, seed, (uint64_t)(c * kblocks + kb), lo32, hi32);
         if (c < C && kb < kblocks)
             *reinterpret_cast<uint2*>(q + c * (T / 2) + kb * 8) = make_uint2(lo32, hi32);
-        sf[(ct * cp + tt) * 512 + (cl & 31) * 16 + (cl >> 5) * 4 + tb] = (uint8_t)sb;
+        sf[((int64_t)ct * cp + tt) * 512 + (cl & 31) * 16 + (cl >> 5) * 4 + tb] = (uint8_t)sb;
     }
 
-    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, const float (&s_enc)[2],
+    __device__ static void phase2(const uint8_t* tile, int32_t tt, int32_t ct, int ctid, const float (&s_enc)[2],
                                   const float (*ftab)[128], const QuantParams& p)
     {
-        quantize_out(tile, t, ctid, s_enc[0], ftab[0], p.mode, p.sr_seed, p.q, p.sf, p);
+        quantize_out(tile, tt, ct, ctid, s_enc[0], ftab[0], p.mode, p.sr_seed, p.q, p.sf, p);
     }
 };
 
@@ -431,10 +413,10 @@ struct OpRht {
 // (token (ctid % 256) / 4, channels 64 (ctid / 256) + 16 (ctid % 4) ..) and
 // the Hadamard column of OpRht.
 struct OpDual {
-    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int64_t tile,
+    __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tt, int32_t ct,
                                  const QuantParams& p)
     {
-        OpRht::issue(m, dst, bar, tile, p);
+        OpRht::issue(m, dst, bar, tt, ct, p);
     }
 
     __device__ static const uint8_t* row_block(const uint8_t* tile, int ctid, uint32_t& row, uint32_t& box,
@@ -452,22 +434,13 @@ struct OpDual {
         const uint8_t* half = row_block(tile, ctid, row, box, blk);
         const uint4 a = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk));
         const uint4 b = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk + 1));
-        uint32_t acc = habs_max2(0u, a.x);
-        acc = habs_max2(acc, a.y);
-        acc = habs_max2(acc, a.z);
-        acc = habs_max2(acc, a.w);
-        acc = habs_max2(acc, b.x);
-        acc = habs_max2(acc, b.y);
-        acc = habs_max2(acc, b.z);
-        acc = habs_max2(acc, b.w);
+        const uint32_t acc = habs_max16(a, b);
         return make_uint2(__float_as_uint(hmax_to_float(acc)), OpRht::transformed_amax(tile, ctid, p));
     }
 
-    __device__ static void phase2(const uint8_t* tile, int64_t t, int ctid, const float (&s_enc)[2],
+    __device__ static void phase2(const uint8_t* tile, int32_t tt, int32_t ct, int ctid, const float (&s_enc)[2],
                                   const float (*ftab)[128], const QuantParams& p)
     {
-        int64_t tt, ct;
-        tile_coords(t, p, tt, ct);
         const int64_t T = p.rows, C = p.cols;
         const int lane = ctid & 31;
         uint32_t row, box, blk;
@@ -476,15 +449,14 @@ struct OpDual {
         const uint4 b = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk + 1));
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         float x[16];
-        uint32_t acc = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             x[2 * j] = bf16lo(w[j]);
             x[2 * j + 1] = bf16hi(w[j]);
-            acc = habs_max2(acc, w[j]);
         }
-        const int64_t tok = tt * 64 + row;
-        const int64_t c0 = ct * 128 + box * 64 + blk * 16;
+        const uint32_t acc = habs_max16(a, b);
+        const int64_t tok = (int64_t)tt * 64 + row;
+        const int64_t c0 = (int64_t)ct * 128 + box * 64 + blk * 16;
         uint32_t lo32, hi32;
         const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc[0], ftab[0], p.mode, p.sr_seed,
                                           (uint64_t)(tok * (C / 16) + c0 / 16), lo32, hi32);
@@ -495,7 +467,7 @@ struct OpDual {
         const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
         const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
         const int64_t cp = (C / 16 + 3) / 4;  // 4-block groups per token row
-        const int64_t kg = ct * 2 + box;      // this 64-channel group
+        const int64_t kg = (int64_t)ct * 2 + box;  // this 64-channel group
         if ((lane & 3) == 0 && kg < cp) {
             const int64_t tr = tok >> 7;      // 128-token row tile of the atom
             const uint32_t r128 = (uint32_t)(tok & 127);
@@ -509,15 +481,63 @@ struct OpDual {
                 *reinterpret_cast<uint32_t*>(p.sf + atom + (rp & 31) * 16 + (rp >> 5) * 4) = 0u;
             }
         }
-        OpRht::quantize_out(tile, t, ctid, s_enc[1], ftab[1], p.mode2, p.sr_seed2, p.q2, p.sf2, p);
+        OpRht::quantize_out(tile, tt, ct, ctid, s_enc[1], ftab[1], p.mode2, p.sr_seed2, p.q2, p.sf2, p);
     }
 };
 
 // ---------------------------------------------------------------- kernel ----
+// Position in a CTA's range of tiles, stepped without divisions: (tr, tc) =
+// (index along the strided axis, along the contiguous axis).
+struct TileCursor {
+    int32_t tr, tc;
+    __device__ __forceinline__ void set(int64_t t, int32_t tiles_c)
+    {
+        tr = (int32_t)(t / tiles_c);
+        tc = (int32_t)(t - (int64_t)tr * tiles_c);
+    }
+    __device__ __forceinline__ void next(int32_t tiles_c)
+    {
+        if (++tc == tiles_c) {
+            tc = 0;
+            ++tr;
+        }
+    }
+    __device__ __forceinline__ void prev(int32_t tiles_c)
+    {
+        if (tc-- == 0) {
+            tc = tiles_c - 1;
+            --tr;
+        }
+    }
+};
+
+// Ring position of load number i: slot i % kMaxStages, and the parity of
+// its use (i / kMaxStages) & 1, stepped without divisions.
+struct RingCursor {
+    uint32_t s, ph;
+    __device__ __forceinline__ void set(uint32_t i)
+    {
+        s = i % kMaxStages;
+        ph = (i / kMaxStages) & 1u;
+    }
+    __device__ __forceinline__ void next()
+    {
+        if (++s == kMaxStages) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// Load sequence of a CTA with n tiles [t_begin, t_begin + n): phase 1 loads
+// them in order (loads 0 .. n-1); the last R stay on chip across the grid
+// barrier; phase 2 re-loads the other n - R in reverse order (loads n ..
+// 2n - R - 1: tile t_begin + n - R - 1 down to t_begin), so the most recently
+// read tiles, likely still in L2, come first.  Phase 2 quantizes load numbers
+// n - R .. 2n - R - 1 in order: the R resident tiles, then the re-loads.
 template <class Op>
 __global__ void __launch_bounds__(kThreads, 1)
-    fused_quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, Workspace* ws,
-                          int stages)
+    fused_quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, Workspace* ws)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -526,9 +546,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t G = gridDim.x, bid = blockIdx.x;
     const int64_t t_begin = p.ntiles * bid / G, t_end = p.ntiles * (bid + 1) / G;
-    const int64_t n = t_end - t_begin;
-    const int64_t R = n < stages ? n : stages;  // tiles kept on chip across the barrier
-    const int64_t total_loads = 2 * n - R;
+    const uint32_t n = (uint32_t)(t_end - t_begin);
+    const uint32_t R = n < (uint32_t)kMaxStages ? n : (uint32_t)kMaxStages;  // tiles kept on chip
+    const uint32_t total_loads = 2 * n - R;
+    const int32_t tiles_c = (int32_t)p.tiles_c;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMaxStages; ++s) {
@@ -544,19 +565,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ producer ----
         if (lane == 0) {
             tma_prefetch_desc(&tmap);
-            int64_t issued = 0;
-            for (int64_t i = 0; i < total_loads; ++i) {
-                const int s = (int)(i % stages);
-                if (i >= stages && !mbar_wait(&ctl->empty[s], (uint32_t)(((i / stages) - 1) & 1), ws, &ctl->abort))
+            RingCursor rc{0, 0};
+            TileCursor tile;
+            tile.set(t_begin, tiles_c);
+            uint32_t issued = 0;
+            for (uint32_t i = 0; i < total_loads; ++i, rc.next()) {
+                if (i == n)  // phase 2 re-loads, from tile t_begin + n - R - 1 down
+                    tile.set(t_begin + n - R - 1, tiles_c);
+                if (i >= (uint32_t)kMaxStages && !mbar_wait(&ctl->empty[rc.s], rc.ph ^ 1u, ws, &ctl->abort))
                     break;
-                const int64_t tile = (i < n) ? t_begin + i : t_begin + (n - R - 1) - (i - n);
-                mbar_expect_tx(&ctl->full[s], kTileBytes);
-                Op::issue(&tmap, smem + (size_t)s * kTileBytes, &ctl->full[s], tile, p);
+                mbar_expect_tx(&ctl->full[rc.s], kTileBytes);
+                Op::issue(&tmap, smem + (size_t)rc.s * kTileBytes, &ctl->full[rc.s], tile.tr, tile.tc, p);
                 ++issued;
+                if (i < n)
+                    tile.next(tiles_c);
+                else
+                    tile.prev(tiles_c);
             }
             // never leave with copies in flight
-            for (int64_t i = issued > stages ? issued - stages : 0; i < issued; ++i)
-                mbar_wait(&ctl->full[i % stages], (uint32_t)((i / stages) & 1), ws, nullptr);
+            RingCursor w;
+            for (uint32_t i = issued > (uint32_t)kMaxStages ? issued - kMaxStages : 0; i < issued; ++i) {
+                w.set(i);
+                mbar_wait(&ctl->full[w.s], w.ph, ws, nullptr);
+            }
         }
         return;
     }
@@ -564,17 +595,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- consumers ----
     const int ctid = threadIdx.x;  // 0 .. kConsumers-1
     uint2 amax_bits = make_uint2(0u, 0u);
-    for (int64_t i = 0; i < n; ++i) {
-        const int s = (int)(i % stages);
-        if (!mbar_wait(&ctl->full[s], (uint32_t)((i / stages) & 1), ws, &ctl->abort))
-            break;
-        const uint2 m = Op::phase1(smem + (size_t)s * kTileBytes, ctid, p);
-        amax_bits.x = max(amax_bits.x, m.x);
-        amax_bits.y = max(amax_bits.y, m.y);
-        if (i < n - R) {
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&ctl->empty[s]);
+    {
+        RingCursor rc{0, 0};
+        for (uint32_t i = 0; i < n; ++i, rc.next()) {
+            if (!mbar_wait(&ctl->full[rc.s], rc.ph, ws, &ctl->abort))
+                break;
+            const uint2 m = Op::phase1(smem + (size_t)rc.s * kTileBytes, ctid, p);
+            amax_bits.x = max(amax_bits.x, m.x);
+            amax_bits.y = max(amax_bits.y, m.y);
+            if (i < n - R) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ctl->empty[rc.s]);
+            }
         }
     }
 #pragma unroll
@@ -628,17 +661,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     named_bar_sync(1, kConsumers);
 
-    volatile int* abort_flag = &ctl->abort;
-    for (int64_t j = 0; j < n && !*abort_flag; ++j) {
-        const int64_t i = (j < R) ? (n - R + j) : (n + j - R);
-        const int s = (int)(i % stages);
-        if (j >= R && !mbar_wait(&ctl->full[s], (uint32_t)((i / stages) & 1), ws, &ctl->abort))
-            break;
-        const int64_t tile = (j < R) ? t_begin + n - R + j : t_begin + (n - R - 1) - (j - R);
-        Op::phase2(smem + (size_t)s * kTileBytes, tile, ctid, s_enc, ctl->ftab, p);
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&ctl->empty[s]);
+    {
+        RingCursor rc;
+        rc.set(n - R);
+        TileCursor tile;
+        tile.set(t_begin + n - R, tiles_c);  // the resident tiles, in order
+        // the resident tiles need no wait; a wait that gives up ends the loop
+        for (uint32_t j = 0; j < n; ++j, rc.next()) {
+            if (j == R)  // then the re-loads, from tile t_begin + n - R - 1 down
+                tile.set(t_begin + n - R - 1, tiles_c);
+            if (j >= R && !mbar_wait(&ctl->full[rc.s], rc.ph, ws, &ctl->abort))
+                break;
+            Op::phase2(smem + (size_t)rc.s * kTileBytes, tile.tr, tile.tc, ctid, s_enc, ctl->ftab, p);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ctl->empty[rc.s]);
+            if (j < R)
+                tile.next(tiles_c);
+            else
+                tile.prev(tiles_c);
+        }
     }
 
     named_bar_sync(1, kConsumers);
@@ -685,8 +727,7 @@ nvfp4_status launch_fused(const CUtensorMap& map, const QuantParams& p, Workspac
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int stages = kMaxStages;
-    if (cudaLaunchKernelEx(&cfg, kern, map, p, ws, stages) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kern, map, p, ws) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     return NVFP4_OK;
 }

@@ -135,10 +135,13 @@ def test_ragged_linear_layer_from_quantizers():
     _check(d, ref, dabs, False, "ragged layer")
 
 
-def test_scale_layout_one_hot():
+@pytest.mark.parametrize("M", [128, 256, 384])
+def test_scale_layout_one_hot(M):
     # Distinct power-of-two scale per (row, 16-block) of A: each output
     # element isolates one scale, so a wrong scale-factor layout shows up.
-    M, N, K = 256, 128, 256
+    # M = 128 runs the one-SM kernel, larger M the paired-SM kernel (both
+    # CTAs' A rows, and a ragged second pair tile at 384).
+    N, K = 128, 256
     rng = np.random.default_rng(5)
     qa = np.full((M, K // 2), 0x22, np.uint8)              # all 1.0
     qb = np.zeros((N, K // 2), np.uint8)
@@ -155,6 +158,35 @@ def test_scale_layout_one_hot():
     for n in range(N):
         for k in range(kb):
             sfb[O.sf_offset(n, k, kb)] = 0x38 + (n // kb) % 4 * 8  # 1, 2, 4, 8
+    ref, dabs = O.gemm_f64(qa, sfa, 1.0, qb, sfb, 1.0, M, N, K)
+    d, st = gemm(qa, sfa, 1.0, qb, sfb, 1.0, M, N, K, out_f32=True)
+    assert st == 0
+    assert np.array_equal(d, ref)
+
+
+@pytest.mark.parametrize("M,N", [(128, 384), (256, 384), (512, 512)])
+def test_scale_layout_one_hot_b(M, N):
+    # The B side: a distinct scale per (row n, 16-block) of B, and A row m
+    # selecting 16-block m % kb, so output (m, n) isolates B's scale of (n,
+    # m % kb).  N = 384 and 512 cover both halves of a pair tile's 256 B rows
+    # (each CTA of a pair stages one half) and a second N tile.
+    K = 256
+    kb = K // 16
+    rng = np.random.default_rng(6)
+    qa = np.zeros((M, K // 2), np.uint8)
+    for m in range(M):
+        blk = m % kb
+        qa[m, blk * 8:(blk + 1) * 8] = 0x22                # A row m selects block m % kb
+    qb = np.full((N, K // 2), 0x22, np.uint8)              # all 1.0
+    sfa = np.zeros(O.sf_bytes(M, K), np.uint8)
+    for r in range(M):
+        for k in range(kb):
+            sfa[O.sf_offset(r, k, kb)] = 0x38
+    sfb = np.zeros(O.sf_bytes(N, K), np.uint8)
+    vals = rng.integers(0x20, 0x50, (N, kb), dtype=np.uint8)
+    for n in range(N):
+        for k in range(kb):
+            sfb[O.sf_offset(n, k, kb)] = vals[n, k]
     ref, dabs = O.gemm_f64(qa, sfa, 1.0, qb, sfb, 1.0, M, N, K)
     d, st = gemm(qa, sfa, 1.0, qb, sfb, 1.0, M, N, K, out_f32=True)
     assert st == 0

@@ -109,11 +109,13 @@ def test_mx_gemm_parity(M, N, K):
         _check(d, ref, dabs, not f32, f"mx {M}x{N}x{K}")
 
 
-def test_mx_gemm_scale_layout_one_hot():
+@pytest.mark.parametrize("M", [128, 256])
+def test_mx_gemm_scale_layout_one_hot(M):
     """A distinct power-of-two scale per (row, 32-block) of A and B rows that
     each select one block: every output isolates one scale byte, so a wrong
-    reading of the scale words (bytes 0 and 1 per 64 elements) shows up."""
-    M, N, K = 128, 128, 256
+    reading of the scale words (bytes 0 and 1 per 64 elements) shows up.
+    M = 128 runs the one-SM kernel, M = 256 the paired-SM kernel."""
+    N, K = 128, 256
     kb = K // 32
     rng = np.random.default_rng(9)
     qa = np.full((M, K // 2), 0x22, np.uint8)  # all 1.0
