@@ -105,6 +105,23 @@ nvfp4_status launch_encode_probe(const float* v, const uint16_t* r, int64_t n, u
     return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+void philox_round_keys(uint64_t seed, uint32_t (&keys)[20])
+{
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        keys[2 * r] = k0;
+        keys[2 * r + 1] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+}
+
+void rht_pair_masks(uint32_t sign_bits, uint32_t (&mask)[16])
+{
+    for (int i = 0; i < 16; ++i)
+        mask[i] = ((sign_bits >> i) & 1u) ? 0x80008000u : 0u;
+}
+
 // 128-row x 64-column tiles, 1x16 blocks along the rows.
 QuantParams params_1x16(int64_t rows, int64_t cols, int mode, uint64_t sr_seed, uint8_t* q, uint8_t* sf,
                         float* g_dec)
@@ -119,6 +136,7 @@ QuantParams params_1x16(int64_t rows, int64_t cols, int mode, uint64_t sr_seed, 
     p.sf = sf;
     p.g_dec = g_dec;
     p.sr_seed = sr_seed;
+    philox_round_keys(sr_seed, p.keys[0]);
     p.mode = mode;
     return p;
 }
@@ -249,14 +267,16 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t T, int64_t C, int64_t ld,
     QuantParams p = {};
     p.rows = T;
     p.cols = C;
-    p.tiles_c = cdiv(C, 128);
+    p.tiles_c = cdiv(C, 256);  // 64-token x 256-channel tiles
     p.tiles_r = cdiv(T, 64);
     p.ntiles = p.tiles_r * p.tiles_c;
     p.q = qT;
     p.sf = sfT;
     p.g_dec = g_dec;
     p.sr_seed = sr_seed;
+    philox_round_keys(sr_seed, p.keys[0]);
     p.rht_signs = rht_sign_bits(rht_seed);
+    rht_pair_masks(p.rht_signs, p.rht_mask);
     p.mode = mode;
     return launch_quantize(QuantKind::kRht, x, ld, p, static_cast<Workspace*>(ws), (cudaStream_t)stream);
 }
@@ -280,7 +300,7 @@ nvfp4_status nvfp4_quantize_dual(const void* x, int64_t T, int64_t C, int64_t ld
     QuantParams p = {};
     p.rows = T;
     p.cols = C;
-    p.tiles_c = cdiv(C, 128);
+    p.tiles_c = cdiv(C, 256);  // 64-token x 256-channel tiles
     p.tiles_r = cdiv(T, 64);
     p.ntiles = p.tiles_r * p.tiles_c;
     p.q = q;
@@ -293,7 +313,10 @@ nvfp4_status nvfp4_quantize_dual(const void* x, int64_t T, int64_t C, int64_t ld
     p.g_dec2 = g_dec_t;
     p.sr_seed2 = sr_seed_t;
     p.mode2 = mode_t;
+    philox_round_keys(sr_seed, p.keys[0]);
+    philox_round_keys(sr_seed_t, p.keys[1]);
     p.rht_signs = rht_sign_bits(rht_seed);
+    rht_pair_masks(p.rht_signs, p.rht_mask);
     return launch_quantize(QuantKind::kDual, x, ld, p, static_cast<Workspace*>(ws), (cudaStream_t)stream);
 }
 

@@ -367,6 +367,27 @@ __device__ __forceinline__ U4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c
     return U4{c0, c1, c2, c3};
 }
 
+// The same generator with the round keys given (keys[2r], keys[2r + 1] for
+// round r: the Weyl sequence of the key, precomputed once per call).
+__device__ __forceinline__ U4 philox4x32_10_keys(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 const uint32_t (&keys)[20])
+{
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t lo0 = 0xD2511F53u * c0;
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ keys[2 * round];
+        const uint32_t n2 = hi0 ^ c3 ^ keys[2 * round + 1];
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return U4{c0, c1, c2, c3};
+}
+
 // ------------------------------------------------------ packed binary32 ----
 // Two binary32 values in one 64-bit register pair; each packed operation is
 // two independent IEEE operations rounded to nearest-even, subnormals kept:

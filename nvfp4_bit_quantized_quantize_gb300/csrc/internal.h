@@ -36,6 +36,8 @@ struct QuantParams {
     float* g_dec;           // tensor decode scale out
     uint64_t sr_seed;
     uint32_t rht_signs;     // 16 sign bits (Hadamard variant)
+    uint32_t rht_mask[16];  // per token i of a 16-block: 0x80008000 where the sign diagonal flips it, else 0
+    uint32_t keys[2][20];   // Philox4x32-10 round keys (k0, k1 of rounds 0..9) of sr_seed and of sr_seed2
     int mode;               // nvfp4_round
     // second output of the dual quantizer (Hadamard, token-major codes)
     uint8_t* q2;
@@ -46,6 +48,13 @@ struct QuantParams {
 };
 
 enum class QuantKind { k1x16, k2d, kRht, kDual };
+
+// Philox4x32-10 round keys of a seed: round r uses (seed lo + r 0x9E3779B9,
+// seed hi + r 0xBB67AE85) (Salmon et al., SC'11), precomputed once per call.
+void philox_round_keys(uint64_t seed, uint32_t (&keys)[20]);
+
+// XOR masks of the random sign diagonal for bf16 pairs (both halves).
+void rht_pair_masks(uint32_t sign_bits, uint32_t (&mask)[16]);
 
 // Launch parameters of the 1x16 quantizer (nvfp4_quantize and its
 // allocation-free variant build them here, so the two cannot drift apart).

@@ -9,10 +9,10 @@
 //   phase 2: per 16-element block: E4M3 block scale, element scaling,
 //            round-to-nearest or stochastic rounding onto E2M1, packed
 //            nibbles and swizzled scale bytes.
-// The last `stages` tiles a CTA read in phase 1 stay in shared memory and are
-// quantized first in phase 2 without a second HBM read; the rest are read
-// again in reverse order, so the most recently read tiles (likely still in
-// L2) come first.
+// The last tiles a CTA read in phase 1 (as many as the ring holds) stay in
+// shared memory and are quantized first in phase 2 without a second HBM read;
+// the rest are read again in reverse order, so the most recently read tiles
+// (likely still in L2) come first.
 //
 // Tile ops:
 //   Op1x16 — 128 rows x 64 cols, 1x16 blocks along rows ("Entrenamiento ...",
@@ -20,11 +20,19 @@
 //   Op2d   — same tile, one scale per 16x16 tile, optional transposed
 //            outputs ("Entrenamiento ...", "Metodología de Entrenamiento":
 //            two-dimensional block scaling for weights).
-//   OpRht  — 64 tokens x 128 channels, 16-point random Hadamard transform
+//   OpRht  — 64 tokens x 256 channels, 16-point random Hadamard transform
 //            along tokens, quantized along tokens and written channel-major
-//            ("Metodología de Entrenamiento": random Hadamard transforms).
+//            ("Metodología de Entrenamiento": random Hadamard transforms);
+//            one thread per channel pair and 16-token block, every butterfly
+//            a packed binary32 operation on the pair.
 //   OpDual — the 1x16 and the Hadamard outputs of one tensor from one read,
 //            each with its own tensor scale (two amaxes reduced in phase 1).
+// The ring holds 224 KB: 14 tiles of 16 KB (1x16, 2-D) or 7 of 32 KB (RHT,
+// dual).  These kernels are bound by the latency of each thread's dependent
+// instruction chain (17 warps per SM, at most 96 registers per thread), not by
+// memory: the loop bookkeeping is kept free of divisions, maxima are trees,
+// and the per-call constants (Philox round keys, sign-diagonal masks) are
+// kernel parameters the host computes.
 //
 // Floating-point order is fixed and identical to the oracle: IEEE division
 // and multiplication with round-to-nearest (__fdiv_rn/__fmul_rn), no FMA
@@ -37,7 +45,7 @@ namespace {
 constexpr int kConsumerWarps = 16;  // one 16-element block per consumer thread per tile
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // last warp is the TMA producer
-constexpr int kTileBytes = 16384;
+constexpr int kRingBytes = 14 * 16384;  // the tile ring: 14 tiles of 16 KB or 7 of 32 KB
 constexpr int kMaxStages = 14;
 
 struct SmemCtl {
@@ -49,7 +57,7 @@ struct SmemCtl {
     int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kMaxStages * kTileBytes + sizeof(SmemCtl);
+constexpr size_t kSmemBytes = 1024 + (size_t)kRingBytes + sizeof(SmemCtl);
 
 // Swizzled (128-byte) address of 16-byte chunk `c` of row `r` in a tile whose
 // rows are 128 bytes.
@@ -75,7 +83,7 @@ __device__ __forceinline__ float div6_rn(float b)
 }
 
 __device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], float bamax, float s_enc,
-                                                  const float* ftab, int mode, uint64_t seed, uint64_t blk,
+                                                  const float* ftab, int mode, const uint32_t (&keys)[20], uint64_t blk,
                                                   uint32_t& lo32, uint32_t& hi32)
 {
     const uint32_t sb = e4m3_rn_sat(__fmul_rn(div6_rn(bamax), s_enc));
@@ -103,8 +111,7 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], float ba
     }
     if (mode == NVFP4_ROUND_SR) {
         // elements 4m..4m+3 round with Philox word m
-        const U4 w = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, (uint32_t)seed,
-                                   (uint32_t)(seed >> 32));
+        const U4 w = philox4x32_10_keys((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, keys);
         lo32 = e2m1x4_sr(v[0], v[1], v[2], v[3], w.x) | (e2m1x4_sr(v[4], v[5], v[6], v[7], w.y) << 16);
         hi32 = e2m1x4_sr(v[8], v[9], v[10], v[11], w.z) | (e2m1x4_sr(v[12], v[13], v[14], v[15], w.w) << 16);
         return sb;
@@ -154,6 +161,8 @@ __device__ __forceinline__ uint32_t scan_tile_bf16(const uint8_t* tile, int ctid
 // Consumer thread ctid owns block (row ctid / 4, block ctid % 4) of the tile;
 // the 4 blocks of a row sit in lanes 4i..4i+3 of one warp.
 struct Op1x16 {
+    static constexpr int kTileBytes = 16384;
+
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tr, int32_t tc,
                                  const QuantParams&)
     {
@@ -183,7 +192,7 @@ struct Op1x16 {
         const int64_t grow = (int64_t)tr * 128 + row;
         const int64_t gcol = (int64_t)tc * 64 + blk * 16;
         uint32_t lo32, hi32;
-        const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc[0], ftab[0], p.mode, p.sr_seed,
+        const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc[0], ftab[0], p.mode, p.keys[0],
                                           (uint64_t)(grow * (p.cols / 16) + gcol / 16), lo32, hi32);
         if (grow < p.rows && gcol < p.cols)
             *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
@@ -222,6 +231,8 @@ __device__ __forceinline__ uint64_t nibble_transpose16(uint64_t w, int i)
 // Each half-warp owns one 16 x 16 tile: lanes 0-15 tile 2w, lanes 16-31 tile
 // 2w + 1 of the 32 tiles (8 row groups x 4 column blocks); lane i has row i.
 struct Op2d {
+    static constexpr int kTileBytes = 16384;
+
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tr, int32_t tc,
                                  const QuantParams& p)
     {
@@ -259,7 +270,7 @@ struct Op2d {
         const int64_t grow = (int64_t)tr * 128 + row;
         const int64_t gcol = (int64_t)tc * 64 + blk * 16;
         uint32_t lo32, hi32;
-        const uint32_t sb = quant_block16(x, __uint_as_float(m), s_enc[0], ftab[0], NVFP4_ROUND_RN, 0, 0, lo32, hi32);
+        const uint32_t sb = quant_block16(x, __uint_as_float(m), s_enc[0], ftab[0], NVFP4_ROUND_RN, p.keys[0], 0, lo32, hi32);
         if (grow < p.rows && gcol < p.cols)
             *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
         p.sf[((int64_t)tr * p.tiles_c + tc) * 512 + (row & 31) * 16 + (row >> 5) * 4 + blk] = (uint8_t)sb;
@@ -286,41 +297,51 @@ struct Op2d {
 };
 
 // ------------------------------------------------------------------- RHT ----
-// Tile = 64 tokens x 128 channels as two 64 x 64 boxes (8 KB each).  Consumer
-// warp w handles token block tb = w / 4 and channels 32 (w % 4) .. + 31, one
-// channel per lane, 16 tokens per thread.
+// Tile = 64 tokens x 256 channels as four 64 x 64 boxes (8 KB each).  The
+// Hadamard work unit is a pair of adjacent channels over one 16-token block:
+// thread ctid takes token block tb = ctid / 128 and channels 2 cp, 2 cp + 1
+// with cp = ctid % 128, so a warp reads whole 128-byte rows of one box (one
+// 32-bit bf16 pair per lane) and every butterfly of every stride is one
+// packed binary32 operation for the two channels.
 struct OpRht {
+    static constexpr int kTileBytes = 32768;
+
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tt, int32_t ct,
                                  const QuantParams&)
     {
-        tma_load_2d(dst, m, bar, ct * 128, tt * 64);
-        tma_load_2d(dst + 8192, m, bar, ct * 128 + 64, tt * 64);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            tma_load_2d(dst + b * 8192, m, bar, ct * 256 + b * 64, tt * 64);
     }
 
-    // D v for this thread's channel and token block, as pairs P[k] =
-    // (element k, element k + 8), and the butterflies of strides 1, 2 and 4:
-    // with that pairing every butterfly of those strides joins lane with
-    // lane, so one packed add and one packed subtract do two of them.
-    __device__ static void butterflies_124(const uint8_t* tile, int ctid, uint32_t signs, uint64_t (&P)[8])
+    // This thread's two channels (cb, cb + 1 of box `box`) and token block.
+    __device__ static void unit(int ctid, uint32_t& tb, uint32_t& box, uint32_t& cb)
     {
-        const int lane = ctid & 31, cw = ctid >> 5;
-        const uint32_t tb = cw >> 2, cl = (cw & 3) * 32 + lane;
-        const uint8_t* half = tile + (cl >> 6) * 8192;
-        const uint32_t cb = cl & 63;
-        float v[16];
+        tb = (uint32_t)ctid >> 7;
+        const uint32_t cp = (uint32_t)ctid & 127u;
+        box = cp >> 5;
+        cb = (cp & 31u) * 2;
+    }
+
+    // D v of both channels as packed pairs P[i] = (channel cb, channel cb + 1)
+    // at token i of the block, then the butterflies of strides 1, 2 and 4.
+    __device__ static void butterflies_124(const uint8_t* tile, int ctid, const uint32_t (&mask)[16],
+                                           uint64_t (&P)[16])
+    {
+        uint32_t tb, box, cb;
+        unit(ctid, tb, box, cb);
+        const uint8_t* bx = tile + box * 8192 + (cb & 7) * 2;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint32_t row = tb * 16 + i;
-            const uint32_t h = *reinterpret_cast<const uint16_t*>(half + sw128(row, cb >> 3) + (cb & 7) * 2);
-            v[i] = __uint_as_float((h << 16) ^ ((signs << (31 - i)) & 0x80000000u));
+            // the sign flip of D, both channels
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(bx + sw128(row, cb >> 3)) ^ mask[i];
+            P[i] = f2_pack(bf16lo(w), bf16hi(w));
         }
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            P[k] = f2_pack(v[k], v[k + 8]);
 #pragma unroll
         for (int hs = 1; hs < 8; hs <<= 1) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 16; ++k) {
                 if (k & hs)
                     continue;
                 const uint64_t a = P[k], b = P[k + hs];
@@ -330,38 +351,42 @@ struct OpRht {
         }
     }
 
-    // y = (1/4) H16 D v for this thread's channel and token block: the
-    // butterflies in stride order 1, 2, 4, 8, then the exact 1/4.
-    __device__ static void transform(const uint8_t* tile, int ctid, uint32_t signs, float (&y)[16])
+    // y = (1/4) H16 D v for both channels: the butterflies in stride order
+    // 1, 2, 4, 8, then the exact 1/4, in place: P[i] = (y of channel cb,
+    // y of channel cb + 1) at token i.
+    __device__ static void transform(const uint8_t* tile, int ctid, const uint32_t (&mask)[16], uint64_t (&P)[16])
     {
-        uint64_t P[8];
-        butterflies_124(tile, ctid, signs, P);
+        butterflies_124(tile, ctid, mask, P);
         const uint64_t quarter = f2_pack(0.25f, 0.25f);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            float a, b;
-            f2_unpack(P[k], a, b);
-            f2_unpack(f2_mul(f2_pack(__fadd_rn(a, b), __fsub_rn(a, b)), quarter), y[k], y[k + 8]);
+            const uint64_t a = P[k], b = P[k + 8];
+            P[k] = f2_mul(f2_add(a, b), quarter);
+            P[k + 8] = f2_mul(f2_sub(a, b), quarter);
         }
     }
 
-    // max |y| as float bits (NaN-propagating).  Multiplying by 1/4 is exact
-    // and monotone, so max |H16 D v| / 4 equals the max over the scaled values.
-    // The last butterfly maps (a, b) to (a + b, a - b), whose larger
-    // magnitude is rn(|a| + |b|) (rounding is monotone and odd); the two
-    // differ only when a and b are both infinite (NaN against Inf), and both
-    // are non-finite.
+    // max |y| over both channels as float bits (NaN-propagating).  Multiplying
+    // by 1/4 is exact and monotone, so max |H16 D v| / 4 equals the max over
+    // the scaled values.  The last butterfly maps (a, b) to (a + b, a - b),
+    // whose larger magnitude is rn(|a| + |b|) (rounding is monotone and odd);
+    // the two differ only when a and b are both infinite (NaN against Inf),
+    // and both are non-finite.
     __device__ static uint32_t transformed_amax(const uint8_t* tile, int ctid, const QuantParams& p)
     {
-        uint64_t P[8];
-        butterflies_124(tile, ctid, p.rht_signs, P);
-        float m = 0.0f;
+        uint64_t P[16];
+        butterflies_124(tile, ctid, p.rht_mask, P);
+        float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            float a, b;
-            f2_unpack(P[k], a, b);
-            asm("max.NaN.f32 %0, %1, %2;" : "=f"(m) : "f"(m), "f"(__fadd_rn(fabsf(a), fabsf(b))));
+            float a0, a1, b0, b1;
+            f2_unpack(P[k], a0, a1);
+            f2_unpack(P[k + 8], b0, b1);
+            asm("max.NaN.f32 %0, %1, %2;" : "=f"(m0) : "f"(m0), "f"(__fadd_rn(fabsf(a0), fabsf(b0))));
+            asm("max.NaN.f32 %0, %1, %2;" : "=f"(m1) : "f"(m1), "f"(__fadd_rn(fabsf(a1), fabsf(b1))));
         }
+        float m;
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(m) : "f"(m0), "f"(m1));
         return __float_as_uint(__fmul_rn(m, 0.25f));
     }
 
@@ -370,37 +395,64 @@ struct OpRht {
         return make_uint2(transformed_amax(tile, ctid, p), 0u);
     }
 
-    // Quantize this thread's transformed channel block into (q, sf) with the
-    // given tensor scale.
-    __device__ static void quantize_out(const uint8_t* tile, int32_t tt, int32_t ct, int ctid, float s_enc,
-                                        const float* ftab, int mode, uint64_t seed, uint8_t* q, uint8_t* sf,
-                                        const QuantParams& p)
+    // Channel w of the transformed pair (w = 0: the lower halves of P) as one
+    // 16-token block of channel c, into (q, sf).
+    __device__ static void put_block(const uint64_t (&P)[16], int w, int64_t c, int64_t kb, float s_enc,
+                                     const float* ftab, int mode, const uint32_t (&keys)[20], uint8_t* q,
+                                     uint8_t* sf, const QuantParams& p)
     {
-        const int lane = ctid & 31, cw = ctid >> 5;
-        const uint32_t tb = cw >> 2, cl = (cw & 3) * 32 + lane;
         const int64_t T = p.rows, C = p.cols;
         const int64_t kblocks = T / 16;
         const int64_t cp = (kblocks + 3) / 4;
         float y[16];
-        transform(tile, ctid, p.rht_signs, y);
-        float bamax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            bamax = fmaxf(bamax, fabsf(y[i]));
-        const int64_t c = (int64_t)ct * 128 + cl;
-        const int64_t kb = (int64_t)tt * 4 + tb;
+        for (int i = 0; i < 16; ++i) {
+            float lo, hi;
+            f2_unpack(P[i], lo, hi);
+            y[i] = w == 0 ? lo : hi;
+        }
+        // max |y| as a tree of depth 4 (a non-finite input is reported, and
+        // its block's outputs are unspecified)
+        float m[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            m[i] = fmaxf(fabsf(y[i]), fabsf(y[i + 8]));
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            m[i] = fmaxf(m[i], m[i + 4]);
+        const float bamax = fmaxf(fmaxf(m[0], m[2]), fmaxf(m[1], m[3]));
         uint32_t lo32, hi32;
-        const uint32_t sb =
-            quant_block16(y, bamax, s_enc, ftab, mode, seed, (uint64_t)(c * kblocks + kb), lo32, hi32);
+        const uint32_t sb = quant_block16(y, bamax, s_enc, ftab, mode, keys, (uint64_t)(c * kblocks + kb), lo32, hi32);
         if (c < C && kb < kblocks)
             *reinterpret_cast<uint2*>(q + c * (T / 2) + kb * 8) = make_uint2(lo32, hi32);
-        sf[((int64_t)ct * cp + tt) * 512 + (cl & 31) * 16 + (cl >> 5) * 4 + tb] = (uint8_t)sb;
+        // rows past C up to the 128-row padding get their zero scale; the
+        // 256-channel tile may reach past the scale buffer's padded rows
+        if (c < ((C + 127) & ~int64_t(127)))
+            sf[((c >> 7) * cp + (kb >> 2)) * 512 + (c & 31) * 16 + ((c & 127) >> 5) * 4 + (kb & 3)] = (uint8_t)sb;
+    }
+
+    // Quantize this thread's two transformed channel blocks into (q, sf) with
+    // the given tensor scale.
+    __device__ static void quantize_out(const uint8_t* tile, int32_t tt, int32_t ct, int ctid, float s_enc,
+                                        const float* ftab, int mode, const uint32_t (&keys)[20], uint8_t* q,
+                                        uint8_t* sf, const QuantParams& p)
+    {
+        uint32_t tb, box, cb;
+        unit(ctid, tb, box, cb);
+        uint64_t P[16];
+        transform(tile, ctid, p.rht_mask, P);
+        const int64_t c = (int64_t)ct * 256 + box * 64 + cb;
+        const int64_t kb = (int64_t)tt * 4 + tb;
+        // one channel after the other keeps the register count in bounds
+#pragma unroll 1
+        for (int w = 0; w < 2; ++w)
+            put_block(P, w, c + w, kb, s_enc, ftab, mode, keys, q, sf, p);
     }
 
     __device__ static void phase2(const uint8_t* tile, int32_t tt, int32_t ct, int ctid, const float (&s_enc)[2],
                                   const float (*ftab)[128], const QuantParams& p)
     {
-        quantize_out(tile, tt, ct, ctid, s_enc[0], ftab[0], p.mode, p.sr_seed, p.q, p.sf, p);
+        quantize_out(tile, tt, ct, ctid, s_enc[0], ftab[0], p.mode, p.keys[0], p.q, p.sf, p);
     }
 };
 
@@ -408,45 +460,49 @@ struct OpRht {
 // Both quantizations of an activation or gradient from one read: 1x16 blocks
 // along channels written row-major (q, sf; the Fprop/Dgrad operand) and the
 // Hadamard-transformed 16-token blocks written channel-major (q2, sf2; the
-// Wgrad operand), each with its own tensor scale.  Tile = 64 tokens x 128
-// channels (the Hadamard op's tile); consumer thread ctid owns the 1x16 block
-// (token (ctid % 256) / 4, channels 64 (ctid / 256) + 16 (ctid % 4) ..) and
-// the Hadamard column of OpRht.
+// Wgrad operand), each with its own tensor scale.  Tile = OpRht's 64 tokens x
+// 256 channels; consumer thread ctid owns two 1x16 blocks, token (ctid % 256)
+// / 4, channels 16 (ctid % 4) .. of boxes ctid / 256 and ctid / 256 + 2, and
+// OpRht's channel pair.
 struct OpDual {
+    static constexpr int kTileBytes = OpRht::kTileBytes;
+
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tt, int32_t ct,
                                  const QuantParams& p)
     {
         OpRht::issue(m, dst, bar, tt, ct, p);
     }
 
-    __device__ static const uint8_t* row_block(const uint8_t* tile, int ctid, uint32_t& row, uint32_t& box,
-                                               uint32_t& blk)
+    __device__ static void row_block(int ctid, uint32_t& row, uint32_t& box0, uint32_t& blk)
     {
-        box = (uint32_t)ctid >> 8;
+        box0 = (uint32_t)ctid >> 8;
         row = ((uint32_t)ctid & 255u) >> 2;
         blk = (uint32_t)ctid & 3u;
-        return tile + box * 8192;
     }
 
     __device__ static uint2 phase1(const uint8_t* tile, int ctid, const QuantParams& p)
     {
-        uint32_t row, box, blk;
-        const uint8_t* half = row_block(tile, ctid, row, box, blk);
-        const uint4 a = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk));
-        const uint4 b = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk + 1));
-        const uint32_t acc = habs_max16(a, b);
+        uint32_t row, box0, blk;
+        row_block(ctid, row, box0, blk);
+        const uint8_t* b0 = tile + box0 * 8192;
+        const uint8_t* b1 = b0 + 2 * 8192;
+        const uint4 a0 = *reinterpret_cast<const uint4*>(b0 + sw128(row, 2 * blk));
+        const uint4 c0 = *reinterpret_cast<const uint4*>(b0 + sw128(row, 2 * blk + 1));
+        const uint4 a1 = *reinterpret_cast<const uint4*>(b1 + sw128(row, 2 * blk));
+        const uint4 c1 = *reinterpret_cast<const uint4*>(b1 + sw128(row, 2 * blk + 1));
+        const uint32_t acc = habs_max2(habs_max16(a0, c0), habs_max16(a1, c1));
         return make_uint2(__float_as_uint(hmax_to_float(acc)), OpRht::transformed_amax(tile, ctid, p));
     }
 
-    __device__ static void phase2(const uint8_t* tile, int32_t tt, int32_t ct, int ctid, const float (&s_enc)[2],
-                                  const float (*ftab)[128], const QuantParams& p)
+    // The 1x16 block of token `row`, channels 16 blk .. of box `box`.
+    __device__ static void row_out(const uint8_t* tile, int32_t tt, int32_t ct, uint32_t row, uint32_t box,
+                                   uint32_t blk, int lane, const float (&s_enc)[2], const float (*ftab)[128],
+                                   const QuantParams& p)
     {
         const int64_t T = p.rows, C = p.cols;
-        const int lane = ctid & 31;
-        uint32_t row, box, blk;
-        const uint8_t* half = row_block(tile, ctid, row, box, blk);
-        const uint4 a = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk));
-        const uint4 b = *reinterpret_cast<const uint4*>(half + sw128(row, 2 * blk + 1));
+        const uint8_t* bx = tile + box * 8192;
+        const uint4 a = *reinterpret_cast<const uint4*>(bx + sw128(row, 2 * blk));
+        const uint4 b = *reinterpret_cast<const uint4*>(bx + sw128(row, 2 * blk + 1));
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         float x[16];
 #pragma unroll
@@ -456,9 +512,9 @@ struct OpDual {
         }
         const uint32_t acc = habs_max16(a, b);
         const int64_t tok = (int64_t)tt * 64 + row;
-        const int64_t c0 = (int64_t)ct * 128 + box * 64 + blk * 16;
+        const int64_t c0 = (int64_t)ct * 256 + box * 64 + blk * 16;
         uint32_t lo32, hi32;
-        const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc[0], ftab[0], p.mode, p.sr_seed,
+        const uint32_t sb = quant_block16(x, hmax_to_float(acc), s_enc[0], ftab[0], p.mode, p.keys[0],
                                           (uint64_t)(tok * (C / 16) + c0 / 16), lo32, hi32);
         if (tok < T && c0 < C)
             *reinterpret_cast<uint2*>(p.q + tok * (C / 2) + c0 / 2) = make_uint2(lo32, hi32);
@@ -466,10 +522,10 @@ struct OpDual {
         const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
         const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
         const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
-        const int64_t cp = (C / 16 + 3) / 4;  // 4-block groups per token row
-        const int64_t kg = (int64_t)ct * 2 + box;  // this 64-channel group
+        const int64_t cp = (C / 16 + 3) / 4;           // 4-block groups per token row
+        const int64_t kg = (int64_t)ct * 4 + box;      // this 64-channel group
         if ((lane & 3) == 0 && kg < cp) {
-            const int64_t tr = tok >> 7;      // 128-token row tile of the atom
+            const int64_t tr = tok >> 7;               // 128-token row tile of the atom
             const uint32_t r128 = (uint32_t)(tok & 127);
             const int64_t atom = (tr * cp + kg) * 512;
             *reinterpret_cast<uint32_t*>(p.sf + atom + (r128 & 31) * 16 + (r128 >> 5) * 4) =
@@ -481,7 +537,17 @@ struct OpDual {
                 *reinterpret_cast<uint32_t*>(p.sf + atom + (rp & 31) * 16 + (rp >> 5) * 4) = 0u;
             }
         }
-        OpRht::quantize_out(tile, tt, ct, ctid, s_enc[1], ftab[1], p.mode2, p.sr_seed2, p.q2, p.sf2, p);
+    }
+
+    __device__ static void phase2(const uint8_t* tile, int32_t tt, int32_t ct, int ctid, const float (&s_enc)[2],
+                                  const float (*ftab)[128], const QuantParams& p)
+    {
+        const int lane = ctid & 31;
+        uint32_t row, box0, blk;
+        row_block(ctid, row, box0, blk);
+        row_out(tile, tt, ct, row, box0, blk, lane, s_enc, ftab, p);
+        row_out(tile, tt, ct, row, box0 + 2, blk, lane, s_enc, ftab, p);
+        OpRht::quantize_out(tile, tt, ct, ctid, s_enc[1], ftab[1], p.mode2, p.keys[1], p.q2, p.sf2, p);
     }
 };
 
@@ -511,18 +577,19 @@ struct TileCursor {
     }
 };
 
-// Ring position of load number i: slot i % kMaxStages, and the parity of
-// its use (i / kMaxStages) & 1, stepped without divisions.
+// Ring position of load number i: slot i % kStages, and the parity of its
+// use (i / kStages) & 1, stepped without divisions.
+template <int kStages>
 struct RingCursor {
     uint32_t s, ph;
     __device__ __forceinline__ void set(uint32_t i)
     {
-        s = i % kMaxStages;
-        ph = (i / kMaxStages) & 1u;
+        s = i % kStages;
+        ph = (i / kStages) & 1u;
     }
     __device__ __forceinline__ void next()
     {
-        if (++s == kMaxStages) {
+        if (++s == kStages) {
             s = 0;
             ph ^= 1u;
         }
@@ -537,22 +604,27 @@ struct RingCursor {
 // n - R .. 2n - R - 1 in order: the R resident tiles, then the re-loads.
 template <class Op>
 __global__ void __launch_bounds__(kThreads, 1)
-    fused_quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, Workspace* ws)
+    fused_quantize_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ QuantParams p,
+                          Workspace* ws)
 {
+    constexpr int kTileBytes = Op::kTileBytes;
+    constexpr int kStages = kRingBytes / kTileBytes;
+    static_assert(kStages <= kMaxStages, "ring");
+    using Ring = RingCursor<kStages>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (size_t)kMaxStages * kTileBytes);
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (size_t)kRingBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t G = gridDim.x, bid = blockIdx.x;
     const int64_t t_begin = p.ntiles * bid / G, t_end = p.ntiles * (bid + 1) / G;
     const uint32_t n = (uint32_t)(t_end - t_begin);
-    const uint32_t R = n < (uint32_t)kMaxStages ? n : (uint32_t)kMaxStages;  // tiles kept on chip
+    const uint32_t R = n < (uint32_t)kStages ? n : (uint32_t)kStages;  // tiles kept on chip
     const uint32_t total_loads = 2 * n - R;
     const int32_t tiles_c = (int32_t)p.tiles_c;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kMaxStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl->full[s], 1);
             mbar_init(&ctl->empty[s], kConsumerWarps);
         }
@@ -565,14 +637,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ producer ----
         if (lane == 0) {
             tma_prefetch_desc(&tmap);
-            RingCursor rc{0, 0};
+            Ring rc{0, 0};
             TileCursor tile;
             tile.set(t_begin, tiles_c);
             uint32_t issued = 0;
             for (uint32_t i = 0; i < total_loads; ++i, rc.next()) {
                 if (i == n)  // phase 2 re-loads, from tile t_begin + n - R - 1 down
                     tile.set(t_begin + n - R - 1, tiles_c);
-                if (i >= (uint32_t)kMaxStages && !mbar_wait(&ctl->empty[rc.s], rc.ph ^ 1u, ws, &ctl->abort))
+                if (i >= (uint32_t)kStages && !mbar_wait(&ctl->empty[rc.s], rc.ph ^ 1u, ws, &ctl->abort))
                     break;
                 mbar_expect_tx(&ctl->full[rc.s], kTileBytes);
                 Op::issue(&tmap, smem + (size_t)rc.s * kTileBytes, &ctl->full[rc.s], tile.tr, tile.tc, p);
@@ -583,8 +655,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tile.prev(tiles_c);
             }
             // never leave with copies in flight
-            RingCursor w;
-            for (uint32_t i = issued > (uint32_t)kMaxStages ? issued - kMaxStages : 0; i < issued; ++i) {
+            Ring w;
+            for (uint32_t i = issued > (uint32_t)kStages ? issued - kStages : 0; i < issued; ++i) {
                 w.set(i);
                 mbar_wait(&ctl->full[w.s], w.ph, ws, nullptr);
             }
@@ -596,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ctid = threadIdx.x;  // 0 .. kConsumers-1
     uint2 amax_bits = make_uint2(0u, 0u);
     {
-        RingCursor rc{0, 0};
+        Ring rc{0, 0};
         for (uint32_t i = 0; i < n; ++i, rc.next()) {
             if (!mbar_wait(&ctl->full[rc.s], rc.ph, ws, &ctl->abort))
                 break;
@@ -662,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(1, kConsumers);
 
     {
-        RingCursor rc;
+        Ring rc;
         rc.set(n - R);
         TileCursor tile;
         tile.set(t_begin + n - R, tiles_c);  // the resident tiles, in order
