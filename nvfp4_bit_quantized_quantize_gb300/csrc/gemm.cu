@@ -393,7 +393,7 @@ struct PairCtl {
     int abort;
 };
 
-constexpr size_t kPSmemBytes = 1024 + (size_t)kPStages * kPStage + kEpilogueWarps * kStoreBufBytes + sizeof(PairCtl);
+constexpr size_t kPSmemBytes = 1024 + (size_t)kPStages * kPStage + kEpilogueWarps * kWideBufBytes + sizeof(PairCtl);
 static_assert(kPStage % 1024 == 0, "stage alignment");
 static_assert(kAccCols + kPSlots * kPSlotStride <= kTmemCols, "tensor memory budget");
 static_assert(kPSmemBytes <= 227 * 1024, "shared memory budget");
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* store_buf = smem + (size_t)kPStages * kPStage;
-    PairCtl* ctl = reinterpret_cast<PairCtl*>(store_buf + kEpilogueWarps * kStoreBufBytes);
+    PairCtl* ctl = reinterpret_cast<PairCtl*>(store_buf + kEpilogueWarps * kWideBufBytes);
     volatile int* abort = &ctl->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t c0 = (int32_t)(tn * PN + half * 128);
             const int32_t row0 = (int32_t)(tm * PM + rank * 128 + q * 32);
             const bool live = c0 < args.N && row0 < args.M;
-            uint8_t* buf = store_buf + (warp - 2) * kStoreBufBytes;
+            uint8_t* buf = store_buf + (warp - 2) * kWideBufBytes;
             const uint32_t taddr = tmem + ((q * 32) << 16) + half * 128;
             if (args.out_f32) {
 #pragma unroll
@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x32(taddr + h * 32, r);
                     tmem_ld_wait();
                     if (live)
-                        epilogue_store_f32(r, alpha, row0, c0 + h * 32, args, buf, &tma_d, lane);
+                        epilogue_store_f32_wide(r, alpha, row0, c0 + h * 32, args, buf, &tma_d, lane);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -667,11 +667,17 @@ nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, 
                               CU_TENSOR_MAP_SWIZZLE_128B))
         return NVFP4_ERR_CUDA;
 
+    // output chunks: 32 rows x 32 bytes, except binary32 output of the
+    // paired-SM kernel: 32 rows x 128 bytes in the 128-byte swizzle (that
+    // epilogue holds the accumulator while it stores, so fewer, larger
+    // stores free it sooner; for bf16 the small chunks measured faster)
     CUtensorMap md;
     const bool f32 = dt == NVFP4_OUT_F32;
+    const bool wide = pair && f32;
     if (!encode_tensor_map_2d(&md, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d,
-                              (uint64_t)N, (uint64_t)M, (uint64_t)ldd * (f32 ? 4u : 2u), f32 ? 8u : 16u, 32u,
-                              CU_TENSOR_MAP_SWIZZLE_NONE))
+                              (uint64_t)N, (uint64_t)M, (uint64_t)ldd * (f32 ? 4u : 2u),
+                              (wide ? 128u : 32u) / (f32 ? 4u : 2u), 32u,
+                              wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
         return NVFP4_ERR_CUDA;
     GemmArgs args{sfa, sfb, ga, gb, d, ldd, (int32_t)M, (int32_t)N, (int32_t)K, dt == NVFP4_OUT_F32 ? 1 : 0};
     CUtensorMap msfa, msfb;

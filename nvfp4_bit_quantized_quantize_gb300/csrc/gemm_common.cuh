@@ -113,4 +113,69 @@ __device__ __forceinline__ void epilogue_store_f32(const uint32_t (&r)[32], floa
     }
 }
 
+// ---- wide chunks (binary32 output of the paired-SM kernel): 32 rows x 128
+// bytes per tensor store, staged in a 4 KB buffer per warp in the store's
+// 128-byte swizzle
+// (16-byte unit u of row r at r * 128 + ((u ^ (r % 8)) * 16), so the eight
+// rows of a quarter-warp's 16-byte writes cover all 32 banks).
+constexpr int kWideBufBytes = 4096;
+
+// Write this lane's 128-byte row (words w[base] .. w[base + 31]) of a chunk of
+// `width` columns at (col, row0), after the previous store has read the
+// buffer, then send it with one tensor store -- or, across the M or N edge,
+// copy each row's elements inside M x N out with plain stores.
+__device__ __forceinline__ void store_wide_chunk(const uint32_t* w, int32_t col, int32_t width, int32_t row0,
+                                                 const GemmArgs& args, uint8_t* buf, const CUtensorMap* tma_d,
+                                                 int lane)
+{
+    if (lane == 0)
+        bulk_wait_read0();
+    __syncwarp();
+    uint8_t* row = buf + lane * 128;
+    const uint32_t r7 = (uint32_t)lane & 7u;
+#pragma unroll
+    for (uint32_t u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(row + ((u ^ r7) << 4)) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+    if (col + width > args.N || row0 + 32 > args.M) {
+        __syncwarp();
+        const int32_t r = row0 + lane;
+        const int es = 128 / width;  // element bytes
+        if (r < args.M) {
+            uint8_t* dst = static_cast<uint8_t*>(args.d) + ((int64_t)r * args.ldd + col) * es;
+#pragma unroll 1
+            for (int e = 0; e < width && col + e < args.N; ++e) {
+                const uint32_t off = (uint32_t)(e * es);
+                const uint8_t* src = row + ((((off >> 4) ^ r7) << 4) | (off & 15u));
+                if (es == 2)
+                    reinterpret_cast<uint16_t*>(dst)[e] = *reinterpret_cast<const uint16_t*>(src);
+                else
+                    reinterpret_cast<uint32_t*>(dst)[e] = *reinterpret_cast<const uint32_t*>(src);
+            }
+        }
+        __syncwarp();
+        return;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tma_d, buf, col, row0);
+        bulk_commit_group();
+    }
+}
+
+// 32 rows x 32 binary32 columns (c0 ..) of accumulator values r times alpha
+// as one chunk.
+__device__ __forceinline__ void epilogue_store_f32_wide(const uint32_t (&r)[32], float alpha, int32_t row0,
+                                                       int32_t c0, const GemmArgs& args, uint8_t* buf,
+                                                       const CUtensorMap* tma_d, int lane)
+{
+    if (c0 >= args.N)
+        return;
+    uint32_t w[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+        w[e] = __float_as_uint(__fmul_rn(__uint_as_float(r[e]), alpha));
+    store_wide_chunk(w, c0, 32, row0, args, buf, tma_d, lane);
+}
+
 }  // namespace nvfp4

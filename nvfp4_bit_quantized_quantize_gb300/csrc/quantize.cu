@@ -773,20 +773,22 @@ template <class Op>
 nvfp4_status launch_fused(const CUtensorMap& map, const QuantParams& p, Workspace* ws, cudaStream_t stream)
 {
     auto kern = fused_quantize_kernel<Op>;
-    static bool attr_set[64] = {};
+    // per device, once: the shared-memory opt-in and the co-resident grid size
+    static int max_grid_of[64] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return NVFP4_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
+    if (max_grid_of[dev] == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
             cudaSuccess)
             return NVFP4_ERR_CUDA;
-        attr_set[dev] = true;
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, kSmemBytes) != cudaSuccess ||
+            occ < 1)
+            return NVFP4_ERR_CUDA;
+        max_grid_of[dev] = occ * device_sm_count();
     }
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, kSmemBytes) != cudaSuccess || occ < 1)
-        return NVFP4_ERR_CUDA;
-    const int64_t max_grid = (int64_t)occ * device_sm_count();
+    const int64_t max_grid = max_grid_of[dev];
     const int grid = (int)(p.ntiles < max_grid ? p.ntiles : max_grid);
 
     cudaLaunchConfig_t cfg = {};
