@@ -30,9 +30,9 @@ def test_gemm_flops_of_the_step():
 
 def test_traffic_reported_only_for_its_source():
     path = os.path.join(bench.ROOT, "profiles", "traffic.json")
-    rec = json.load(open(path))["nvf4_gemm_kernel"]
-    assert bench.traffic_for("nvf4_gemm_kernel", rec["source_hash"]) == pytest.approx(rec["dram_bytes_per_launch"])
-    assert bench.traffic_for("nvf4_gemm_kernel", "0" * 16) is None
+    rec = json.load(open(path))["nvf4_gemm_pair_kernel"]
+    assert bench.traffic_for("nvf4_gemm_pair_kernel", rec["source_hash"]) == pytest.approx(rec["dram_bytes_per_launch"])
+    assert bench.traffic_for("nvf4_gemm_pair_kernel", "0" * 16) is None
     assert bench.traffic_for("no_such_kernel", rec["source_hash"]) is None
     # the hash covers every file the kernel is built from
     h = bench.source_hash(bench.GEMM_SOURCES)
