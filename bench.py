@@ -64,11 +64,12 @@ def peaks():
 def quant_bytes(kind: str, rows: int, cols: int) -> float:
     """Algorithmic HBM bytes of one quantizer launch: bf16 read once (twice when
     the tensor exceeds half the L2, since the tensor amax must be known before
-    any code is written), plus packed codes and scale bytes written."""
+    any code is written -- unless the amaxes are given), plus packed codes and
+    scale bytes written."""
     n = rows * cols
-    reads = 1 if 2 * n <= 0.5 * L2_BYTES else 2
+    reads = 1 if kind.endswith("_from_amax") or 2 * n <= 0.5 * L2_BYTES else 2
     out = n / 2 + n / 16
-    if kind in ("quantize_2d_t", "quantize_dual"):
+    if kind in ("quantize_2d_t", "quantize_dual", "quantize_dual_from_amax"):
         out *= 2
     return reads * 2.0 * n + out
 

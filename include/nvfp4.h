@@ -163,6 +163,22 @@ nvfp4_status nvfp4_quantize_dual(const void* x, int64_t T, int64_t C, int64_t ld
                                  void* ws, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_dual with both tensor amaxes given: amax (2 floats of
+ * DEVICE memory, 4-byte aligned) holds max |x| and the Hadamard form's max
+ * |y| as nvfp4_gemm_amax writes them for its output.  The kernel skips its
+ * reduction pass and the grid-wide barrier and reads x once.  Every output is
+ * what nvfp4_quantize_dual writes when the given values are the true
+ * maxima; a non-finite amax is reported as NVFP4_ERR_NONFINITE.
+ */
+nvfp4_status nvfp4_quantize_dual_from_amax(const void* x, int64_t T, int64_t C, int64_t ld,
+                                           const float* amax,
+                                           nvfp4_round mode, uint64_t sr_seed,
+                                           uint8_t* q, uint8_t* sf, float* g_dec,
+                                           uint64_t rht_seed, nvfp4_round mode_t, uint64_t sr_seed_t,
+                                           uint8_t* qT, uint8_t* sfT, float* g_dec_t,
+                                           void* ws, nvfp4_stream_t stream);
+
+/*
  * Quantization-noise meter ["FP4 All the Way", "Describir": quantized
  * training loses efficiency once the gradient norm falls below about
  * sqrt(3) times the quantization noise].  For x [rows, cols] (bf16, leading
@@ -207,6 +223,36 @@ nvfp4_status nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga,
                         int64_t M, int64_t N, int64_t K,
                         void* d, int64_t ldd, nvfp4_out_dtype out_dtype,
                         void* ws, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm with bf16 output that also reduces the two tensor amaxes the
+ * quantization of its output needs, so that nvfp4_quantize_dual_from_amax can
+ * quantize D in one pass instead of reading it twice [multi-level scaling:
+ * the tensor scale comes from the tensor's amax, "I ricercatori di Nvidia
+ * ...", "Come funziona NVFP4?"; the Wgrad form is Hadamard-transformed along
+ * tokens, "Entrenamiento ...", "Metodología de Entrenamiento"].  Rows of D
+ * are tokens, columns channels.
+ *   amax    out: 2 floats of DEVICE memory (4-byte aligned), written when the
+ *           GEMM ends:
+ *             amax[0] = max |D| over the bf16 output,
+ *             amax[1] = max |y| over y = (1/4) H16 S v for every 16-row block
+ *                       v of every column of D (S from rht_seed, as
+ *                       nvfp4_rht_quantize; butterflies with strides 1, 2, 4,
+ *                       8 in binary32),
+ *           bit-identical to the amaxes nvfp4_quantize_dual computes from D
+ *           with the same rht_seed.  A non-finite D gives a non-finite amax,
+ *           which the quantizer reports.
+ * Arguments otherwise as nvfp4_gemm with out_dtype = NVFP4_OUT_BF16.
+ * M % 16 == 0 and N % 16 == 0 (the shapes the dual quantizer takes).  Runs on
+ * the paired-SM kernel for every M.  The workspace carries the partial
+ * maxima while the GEMM runs (the last CTA clears them): one call at a time
+ * per workspace, as for every call.
+ */
+nvfp4_status nvfp4_gemm_amax(const uint8_t* a, const uint8_t* sfa, const float* ga,
+                             const uint8_t* b, const uint8_t* sfb, const float* gb,
+                             int64_t M, int64_t N, int64_t K,
+                             void* d, int64_t ldd, uint64_t rht_seed, float* amax,
+                             void* ws, nvfp4_stream_t stream);
 
 /*
  * MXFP4, the comparison format ["I ricercatori di Nvidia sbloccano ...",

@@ -26,7 +26,7 @@ STATUS = {0: "OK", 1: "ERR_ARG", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_NONFINI
 EXPORTS = ["nvfp4_sf_bytes", "nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_quantize",
            "nvfp4_quantize_2d", "nvfp4_rht_quantize", "nvfp4_quantize_dual", "nvfp4_quant_noise", "nvfp4_gemm",
            "nvfp4_mxfp4_quantize", "nvfp4_mxfp4_gemm", "nvfp4_device_status", "nvfp4_status_str",
-           "nvfp4_encode_probe", "nvfp4_quantize_noalloc"]
+           "nvfp4_encode_probe", "nvfp4_quantize_noalloc", "nvfp4_gemm_amax", "nvfp4_quantize_dual_from_amax"]
 
 
 class NVFP4Error(RuntimeError):
@@ -64,6 +64,9 @@ def load() -> ctypes.CDLL:
         "nvfp4_status_str": ([i32], ctypes.c_char_p),
         "nvfp4_encode_probe": ([p, p, i64, p, p, p, p], i32),
         "nvfp4_quantize_noalloc": ([p, i64, i64, i64, i32, u64, p, p, p, p], i32),
+        "nvfp4_gemm_amax": ([p, p, p, p, p, p, i64, i64, i64, p, i64, u64, p, p, p], i32),
+        "nvfp4_quantize_dual_from_amax": ([p, i64, i64, i64, p, i32, u64, p, p, p, u64, i32, u64, p, p, p, p, p],
+                                          i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -146,6 +149,19 @@ def nvfp4_quantize_dual(x, T, C, ld, mode, sr_seed, q, sf, g_dec, rht_seed, mode
     _check("nvfp4_quantize_dual", load().nvfp4_quantize_dual(
         _ptr(x), T, C, ld, mode, sr_seed, _ptr(q), _ptr(sf), _ptr(g_dec), rht_seed, mode_t, sr_seed_t,
         _ptr(qT), _ptr(sfT), _ptr(g_dec_t), _ptr(ws), _stream(stream)))
+
+
+def nvfp4_quantize_dual_from_amax(x, T, C, ld, amax, mode, sr_seed, q, sf, g_dec, rht_seed, mode_t, sr_seed_t,
+                                  qT, sfT, g_dec_t, ws, stream=None) -> None:
+    _check("nvfp4_quantize_dual_from_amax", load().nvfp4_quantize_dual_from_amax(
+        _ptr(x), T, C, ld, _ptr(amax), mode, sr_seed, _ptr(q), _ptr(sf), _ptr(g_dec), rht_seed, mode_t,
+        sr_seed_t, _ptr(qT), _ptr(sfT), _ptr(g_dec_t), _ptr(ws), _stream(stream)))
+
+
+def nvfp4_gemm_amax(a, sfa, ga, b, sfb, gb, M, N, K, d, ldd, rht_seed, amax, ws, stream=None) -> None:
+    _check("nvfp4_gemm_amax", load().nvfp4_gemm_amax(
+        _ptr(a), _ptr(sfa), _ptr(ga), _ptr(b), _ptr(sfb), _ptr(gb), M, N, K, _ptr(d), ldd, rht_seed,
+        _ptr(amax), _ptr(ws), _stream(stream)))
 
 
 def nvfp4_gemm(a, sfa, ga, b, sfb, gb, M, N, K, d, ldd, out_dtype, ws, stream=None) -> None:

@@ -185,6 +185,47 @@ uint32_t rht_sign_bits(uint64_t rht_seed)
     return c[0] & 0xFFFFu;
 }
 
+// Both forms of nvfp4_quantize_dual; amax (device, 2 floats) given or nullptr.
+nvfp4_status quantize_dual(const void* x, int64_t T, int64_t C, int64_t ld, nvfp4_round mode, uint64_t sr_seed,
+                           uint8_t* q, uint8_t* sf, float* g_dec, uint64_t rht_seed, nvfp4_round mode_t,
+                           uint64_t sr_seed_t, uint8_t* qT, uint8_t* sfT, float* g_dec_t, const float* amax, void* ws,
+                           nvfp4_stream_t stream)
+{
+    if (!x || !q || !sf || !g_dec || !qT || !sfT || !g_dec_t || !ws ||
+        (mode != NVFP4_ROUND_RN && mode != NVFP4_ROUND_SR) || (mode_t != NVFP4_ROUND_RN && mode_t != NVFP4_ROUND_SR))
+        return NVFP4_ERR_ARG;
+    if (T <= 0 || C <= 0 || T % 16 != 0 || C % 16 != 0 || ld < C || T > (1ll << 31) || C > (1ll << 31))
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sf) || !aligned16(qT) || !aligned16(sfT) || !aligned16(ws) ||
+        ld % 8 != 0)
+        return NVFP4_ERR_ALIGN;
+    nvfp4_status st = check_device();
+    if (st != NVFP4_OK)
+        return st;
+    QuantParams p = {};
+    p.rows = T;
+    p.cols = C;
+    p.tiles_c = cdiv(C, 256);  // 64-token x 256-channel tiles
+    p.tiles_r = cdiv(T, 64);
+    p.ntiles = p.tiles_r * p.tiles_c;
+    p.q = q;
+    p.sf = sf;
+    p.g_dec = g_dec;
+    p.sr_seed = sr_seed;
+    p.mode = mode;
+    p.q2 = qT;
+    p.sf2 = sfT;
+    p.g_dec2 = g_dec_t;
+    p.sr_seed2 = sr_seed_t;
+    p.mode2 = mode_t;
+    p.amax_in = amax;
+    philox_round_keys(sr_seed, p.keys[0]);
+    philox_round_keys(sr_seed_t, p.keys[1]);
+    p.rht_signs = rht_sign_bits(rht_seed);
+    rht_pair_masks(p.rht_signs, p.rht_mask);
+    return launch_quantize(QuantKind::kDual, x, ld, p, static_cast<Workspace*>(ws), (cudaStream_t)stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -286,38 +327,22 @@ nvfp4_status nvfp4_quantize_dual(const void* x, int64_t T, int64_t C, int64_t ld
                                  nvfp4_round mode_t, uint64_t sr_seed_t, uint8_t* qT, uint8_t* sfT, float* g_dec_t,
                                  void* ws, nvfp4_stream_t stream)
 {
-    if (!x || !q || !sf || !g_dec || !qT || !sfT || !g_dec_t || !ws ||
-        (mode != NVFP4_ROUND_RN && mode != NVFP4_ROUND_SR) || (mode_t != NVFP4_ROUND_RN && mode_t != NVFP4_ROUND_SR))
+    return quantize_dual(x, T, C, ld, mode, sr_seed, q, sf, g_dec, rht_seed, mode_t, sr_seed_t, qT, sfT, g_dec_t,
+                         nullptr, ws, stream);
+}
+
+nvfp4_status nvfp4_quantize_dual_from_amax(const void* x, int64_t T, int64_t C, int64_t ld, const float* amax,
+                                           nvfp4_round mode, uint64_t sr_seed, uint8_t* q, uint8_t* sf,
+                                           float* g_dec, uint64_t rht_seed, nvfp4_round mode_t, uint64_t sr_seed_t,
+                                           uint8_t* qT, uint8_t* sfT, float* g_dec_t, void* ws,
+                                           nvfp4_stream_t stream)
+{
+    if (!amax)
         return NVFP4_ERR_ARG;
-    if (T <= 0 || C <= 0 || T % 16 != 0 || C % 16 != 0 || ld < C || T > (1ll << 31) || C > (1ll << 31))
-        return NVFP4_ERR_SHAPE;
-    if (!aligned16(x) || !aligned16(q) || !aligned16(sf) || !aligned16(qT) || !aligned16(sfT) || !aligned16(ws) ||
-        ld % 8 != 0)
+    if (reinterpret_cast<uintptr_t>(amax) & 3)
         return NVFP4_ERR_ALIGN;
-    nvfp4_status st = check_device();
-    if (st != NVFP4_OK)
-        return st;
-    QuantParams p = {};
-    p.rows = T;
-    p.cols = C;
-    p.tiles_c = cdiv(C, 256);  // 64-token x 256-channel tiles
-    p.tiles_r = cdiv(T, 64);
-    p.ntiles = p.tiles_r * p.tiles_c;
-    p.q = q;
-    p.sf = sf;
-    p.g_dec = g_dec;
-    p.sr_seed = sr_seed;
-    p.mode = mode;
-    p.q2 = qT;
-    p.sf2 = sfT;
-    p.g_dec2 = g_dec_t;
-    p.sr_seed2 = sr_seed_t;
-    p.mode2 = mode_t;
-    philox_round_keys(sr_seed, p.keys[0]);
-    philox_round_keys(sr_seed_t, p.keys[1]);
-    p.rht_signs = rht_sign_bits(rht_seed);
-    rht_pair_masks(p.rht_signs, p.rht_mask);
-    return launch_quantize(QuantKind::kDual, x, ld, p, static_cast<Workspace*>(ws), (cudaStream_t)stream);
+    return quantize_dual(x, T, C, ld, mode, sr_seed, q, sf, g_dec, rht_seed, mode_t, sr_seed_t, qT, sfT, g_dec_t,
+                         amax, ws, stream);
 }
 
 nvfp4_status nvfp4_quant_noise(const void* x, int64_t rows, int64_t cols, int64_t ld, const uint8_t* q,
@@ -353,8 +378,28 @@ nvfp4_status nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, c
     nvfp4_status st = check_device();
     if (st != NVFP4_OK)
         return st;
-    return launch_gemm(a, sfa, ga, b, sfb, gb, M, N, K, d, ldd, out_dtype, false, static_cast<Workspace*>(ws),
-                       (cudaStream_t)stream);
+    return launch_gemm(a, sfa, ga, b, sfb, gb, M, N, K, d, ldd, out_dtype, false, nullptr, 0u,
+                       static_cast<Workspace*>(ws), (cudaStream_t)stream);
+}
+
+nvfp4_status nvfp4_gemm_amax(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
+                             const uint8_t* sfb, const float* gb, int64_t M, int64_t N, int64_t K, void* d,
+                             int64_t ldd, uint64_t rht_seed, float* amax, void* ws, nvfp4_stream_t stream)
+{
+    if (!a || !sfa || !ga || !b || !sfb || !gb || !d || !ws || !amax)
+        return NVFP4_ERR_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || K % 32 != 0 || M % 16 != 0 || N % 16 != 0 || ldd < N ||
+        K / 2 >= (1ll << 32) || M > (1ll << 31) || N > (1ll << 31))
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d) || !aligned16(ws) ||
+        (ldd * 2) % 16 != 0 || (reinterpret_cast<uintptr_t>(ga) & 3) || (reinterpret_cast<uintptr_t>(gb) & 3) ||
+        (reinterpret_cast<uintptr_t>(amax) & 3))
+        return NVFP4_ERR_ALIGN;
+    nvfp4_status st = check_device();
+    if (st != NVFP4_OK)
+        return st;
+    return launch_gemm(a, sfa, ga, b, sfb, gb, M, N, K, d, ldd, NVFP4_OUT_BF16, false, amax,
+                       rht_sign_bits(rht_seed), static_cast<Workspace*>(ws), (cudaStream_t)stream);
 }
 
 nvfp4_status nvfp4_mxfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q, uint8_t* sf,
@@ -387,7 +432,7 @@ nvfp4_status nvfp4_mxfp4_gemm(const uint8_t* a, const uint8_t* sfa, const uint8_
     nvfp4_status st = check_device();
     if (st != NVFP4_OK)
         return st;
-    return launch_gemm(a, sfa, nullptr, b, sfb, nullptr, M, N, K, d, ldd, out_dtype, true,
+    return launch_gemm(a, sfa, nullptr, b, sfb, nullptr, M, N, K, d, ldd, out_dtype, true, nullptr, 0u,
                        static_cast<Workspace*>(ws), (cudaStream_t)stream);
 }
 

@@ -397,6 +397,7 @@ constexpr size_t kPSmemBytes = 1024 + (size_t)kPStages * kPStage + kEpilogueWarp
 static_assert(kPStage % 1024 == 0, "stage alignment");
 static_assert(kAccCols + kPSlots * kPSlotStride <= kTmemCols, "tensor memory budget");
 static_assert(kPSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kStoreBufBytes + kRhtBufBytes <= kWideBufBytes, "epilogue buffer: bf16 chunk + Hadamard scratch");
 
 constexpr uint32_t kIdescNvf4Pair = mma_idesc<false>(PM, PN);
 constexpr uint32_t kIdescMxf4Pair = mma_idesc<true>(PM, PN);
@@ -534,6 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t half = (warp - 2) >> 2;   // columns 128*half .. +127
         const float alpha = kMx ? 1.0f : __fmul_rn(*args.ga, *args.gb);
         const uint32_t empty_addr = mapa_shared(smem_u32(&ctl->tmem_empty), 0);
+        const bool amax_on = !kMx && args.amax_out != nullptr;
+        uint32_t* rbuf = reinterpret_cast<uint32_t*>(store_buf + (warp - 2) * kWideBufBytes + kStoreBufBytes);
+        uint32_t rmax = 0;
+        float tmax = 0.0f;
         for (uint32_t n = 0; n < my_tiles && !*abort; ++n) {
             const uint32_t t = cluster + n * nclusters;
             const uint32_t tm = t % tiles_m, tn = t / tiles_m;
@@ -579,10 +584,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive_remote(empty_addr);
-                if (live)
+                // (with the output maxima, folded in as the chunks leave)
+                if (live && amax_on)
+                    epilogue_store_bf16_amax(p, row0, c0, args, buf, rbuf, &tma_d, lane, rmax, tmax);
+                else if (live)
                     epilogue_store_bf16(p, row0, c0, args, buf, &tma_d, lane);
             }
         }
+        // every epilogue warp reports, even one that stopped early
+        if (amax_on)
+            epilogue_amax_finish(rmax, tmax, args, ws, gridDim.x * kEpilogueWarps, lane);
         if (lane == 0)
             bulk_wait_all();
     } else if (warp >= kFirstScaleWarp) {
@@ -653,11 +664,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
                          const uint8_t* sfb, const float* gb, int64_t M, int64_t N, int64_t K, void* d,
-                         int64_t ldd, nvfp4_out_dtype dt, bool mx, Workspace* ws, cudaStream_t stream)
+                         int64_t ldd, nvfp4_out_dtype dt, bool mx, float* amax_out, uint32_t rht_signs,
+                         Workspace* ws, cudaStream_t stream)
 {
     // 256-row pair tiles; a matrix of at most 128 rows would leave one SM of
-    // every pair without A rows, so it runs on the one-SM kernel
-    const bool pair = M > 128;
+    // every pair without A rows, so it runs on the one-SM kernel -- unless
+    // the output maxima are wanted, which only the paired kernel reduces
+    // (rows past M read as zeros there, so any M is correct on it)
+    const bool pair = M > 128 || amax_out != nullptr;
     CUtensorMap ma, mb;
     if (!encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(K / 2),
                               (uint64_t)M, (uint64_t)(K / 2), 128u, (uint32_t)BM, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -679,7 +693,8 @@ nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, 
                               (wide ? 128u : 32u) / (f32 ? 4u : 2u), 32u,
                               wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
         return NVFP4_ERR_CUDA;
-    GemmArgs args{sfa, sfb, ga, gb, d, ldd, (int32_t)M, (int32_t)N, (int32_t)K, dt == NVFP4_OUT_F32 ? 1 : 0};
+    GemmArgs args{sfa, sfb, ga, gb, d, ldd, (int32_t)M, (int32_t)N, (int32_t)K, dt == NVFP4_OUT_F32 ? 1 : 0,
+                  amax_out, rht_signs};
     CUtensorMap msfa, msfb;
     if (!encode_sf_atom_map(&msfa, sfa, M, K, 1) || !encode_sf_atom_map(&msfb, sfb, N, K, 2))
         return NVFP4_ERR_CUDA;

@@ -17,7 +17,9 @@ struct Workspace {
     uint32_t arrived;     // CTAs that reached the grid barrier
     uint32_t departed;    // CTAs that finished
     uint32_t amax2_bits;  // second output's amax (dual quantizer: max |RHT(x)|)
-    uint32_t pad[59];
+    uint32_t gemm_amax[2];  // GEMM with output maxima: max |D| and max |RHT(D)| so far, as float bits
+    uint32_t gemm_done;     // GEMM epilogue warps that added their maxima
+    uint32_t pad[56];
 };
 static_assert(sizeof(Workspace) == 256, "workspace layout");
 
@@ -45,6 +47,9 @@ struct QuantParams {
     float* g_dec2;
     uint64_t sr_seed2;
     int mode2;
+    // the tensor amaxes (both outputs' for the dual quantizer), already
+    // reduced on the device by the producer of x; nullptr: reduce them here
+    const float* amax_in;
 };
 
 enum class QuantKind { k1x16, k2d, kRht, kDual };
@@ -68,7 +73,8 @@ nvfp4_status launch_quantize(QuantKind kind, const void* x, int64_t ld, const Qu
 
 nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
                          const uint8_t* sfb, const float* gb, int64_t M, int64_t N, int64_t K, void* d,
-                         int64_t ldd, nvfp4_out_dtype dt, bool mx, Workspace* ws, cudaStream_t stream);
+                         int64_t ldd, nvfp4_out_dtype dt, bool mx, float* amax_out, uint32_t rht_signs,
+                         Workspace* ws, cudaStream_t stream);
 
 nvfp4_status launch_mxfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q, uint8_t* sf,
                                    Workspace* ws, cudaStream_t stream);

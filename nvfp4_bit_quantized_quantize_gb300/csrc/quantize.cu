@@ -12,7 +12,9 @@
 // The last tiles a CTA read in phase 1 (as many as the ring holds) stay in
 // shared memory and are quantized first in phase 2 without a second HBM read;
 // the rest are read again in reverse order, so the most recently read tiles
-// (likely still in L2) come first.
+// (likely still in L2) come first.  When the amaxes are given (the GEMM that
+// wrote x reduced them in its epilogue), phase 1 and the barrier are skipped
+// and every tile is read once.
 //
 // Tile ops:
 //   Op1x16 — 128 rows x 64 cols, 1x16 blocks along rows ("Entrenamiento ...",
@@ -619,7 +621,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t G = gridDim.x, bid = blockIdx.x;
     const int64_t t_begin = p.ntiles * bid / G, t_end = p.ntiles * (bid + 1) / G;
     const uint32_t n = (uint32_t)(t_end - t_begin);
-    const uint32_t R = n < (uint32_t)kStages ? n : (uint32_t)kStages;  // tiles kept on chip
+    // amaxes given: no phase 1 and no barrier; the tiles are read once, in
+    // order (every formula below with R = n)
+    const bool given = p.amax_in != nullptr;
+    const uint32_t R = given ? n : (n < (uint32_t)kStages ? n : (uint32_t)kStages);  // tiles kept on chip
     const uint32_t total_loads = 2 * n - R;
     const int32_t tiles_c = (int32_t)p.tiles_c;
 
@@ -666,56 +671,70 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------------------------------------- consumers ----
     const int ctid = threadIdx.x;  // 0 .. kConsumers-1
-    uint2 amax_bits = make_uint2(0u, 0u);
-    {
-        Ring rc{0, 0};
-        for (uint32_t i = 0; i < n; ++i, rc.next()) {
-            if (!mbar_wait(&ctl->full[rc.s], rc.ph, ws, &ctl->abort))
-                break;
-            const uint2 m = Op::phase1(smem + (size_t)rc.s * kTileBytes, ctid, p);
-            amax_bits.x = max(amax_bits.x, m.x);
-            amax_bits.y = max(amax_bits.y, m.y);
-            if (i < n - R) {
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&ctl->empty[rc.s]);
+    if (given) {
+        if (ctid == 0) {
+            // maxima of magnitudes: a sign bit is dropped; a non-finite
+            // amax is reported and quantizes as 0 (all-zero outputs)
+            float a0 = fabsf(p.amax_in[0]), a1 = fabsf(p.amax_in[1]);
+            if (__float_as_uint(a0) >= 0x7F800000u || __float_as_uint(a1) >= 0x7F800000u) {
+                record_status(ws, NVFP4_ERR_NONFINITE);
+                a0 = a1 = 0.0f;
+            }
+            ctl->amax[0] = a0;
+            ctl->amax[1] = a1;
+        }
+    } else {
+        uint2 amax_bits = make_uint2(0u, 0u);
+        {
+            Ring rc{0, 0};
+            for (uint32_t i = 0; i < n; ++i, rc.next()) {
+                if (!mbar_wait(&ctl->full[rc.s], rc.ph, ws, &ctl->abort))
+                    break;
+                const uint2 m = Op::phase1(smem + (size_t)rc.s * kTileBytes, ctid, p);
+                amax_bits.x = max(amax_bits.x, m.x);
+                amax_bits.y = max(amax_bits.y, m.y);
+                if (i < n - R) {
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&ctl->empty[rc.s]);
+                }
             }
         }
-    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        amax_bits.x = max(amax_bits.x, __shfl_xor_sync(0xFFFFFFFFu, amax_bits.x, off));
-        amax_bits.y = max(amax_bits.y, __shfl_xor_sync(0xFFFFFFFFu, amax_bits.y, off));
-    }
-    if (lane == 0) {
-        ctl->warp_amax[0][warp] = amax_bits.x;
-        ctl->warp_amax[1][warp] = amax_bits.y;
-    }
-    named_bar_sync(1, kConsumers);
-    if (ctid == 0) {
-        uint32_t m0 = 0, m1 = 0;
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            m0 = max(m0, ctl->warp_amax[0][w]);
-            m1 = max(m1, ctl->warp_amax[1][w]);
+        for (int off = 16; off > 0; off >>= 1) {
+            amax_bits.x = max(amax_bits.x, __shfl_xor_sync(0xFFFFFFFFu, amax_bits.x, off));
+            amax_bits.y = max(amax_bits.y, __shfl_xor_sync(0xFFFFFFFFu, amax_bits.y, off));
         }
-        atomicMax(&ws->amax_bits, m0);
-        atomicMax(&ws->amax2_bits, m1);
-        __threadfence();
-        atomicAdd(&ws->arrived, 1u);
-        const uint64_t t0 = global_ns();
-        while (ld_acquire_gpu(&ws->arrived) < (uint32_t)G) {
-            if (global_ns() - t0 > kWaitLimitNs) {
-                record_status(ws, NVFP4_ERR_TIMEOUT);
-                break;
+        if (lane == 0) {
+            ctl->warp_amax[0][warp] = amax_bits.x;
+            ctl->warp_amax[1][warp] = amax_bits.y;
+        }
+        named_bar_sync(1, kConsumers);
+        if (ctid == 0) {
+            uint32_t m0 = 0, m1 = 0;
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                m0 = max(m0, ctl->warp_amax[0][w]);
+                m1 = max(m1, ctl->warp_amax[1][w]);
             }
-            __nanosleep(64);
+            atomicMax(&ws->amax_bits, m0);
+            atomicMax(&ws->amax2_bits, m1);
+            __threadfence();
+            atomicAdd(&ws->arrived, 1u);
+            const uint64_t t0 = global_ns();
+            while (ld_acquire_gpu(&ws->arrived) < (uint32_t)G) {
+                if (global_ns() - t0 > kWaitLimitNs) {
+                    record_status(ws, NVFP4_ERR_TIMEOUT);
+                    break;
+                }
+                __nanosleep(64);
+            }
+            const uint32_t am0 = ld_acquire_gpu(&ws->amax_bits);
+            const uint32_t am1 = ld_acquire_gpu(&ws->amax2_bits);
+            if (am0 >= 0x7F800000u || am1 >= 0x7F800000u)
+                record_status(ws, NVFP4_ERR_NONFINITE);
+            ctl->amax[0] = __uint_as_float(am0);
+            ctl->amax[1] = __uint_as_float(am1);
         }
-        const uint32_t am0 = ld_acquire_gpu(&ws->amax_bits);
-        const uint32_t am1 = ld_acquire_gpu(&ws->amax2_bits);
-        if (am0 >= 0x7F800000u || am1 >= 0x7F800000u)
-            record_status(ws, NVFP4_ERR_NONFINITE);
-        ctl->amax[0] = __uint_as_float(am0);
-        ctl->amax[1] = __uint_as_float(am1);
     }
     named_bar_sync(1, kConsumers);
 
@@ -742,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t j = 0; j < n; ++j, rc.next()) {
             if (j == R)  // then the re-loads, from tile t_begin + n - R - 1 down
                 tile.set(t_begin + n - R - 1, tiles_c);
-            if (j >= R && !mbar_wait(&ctl->full[rc.s], rc.ph, ws, &ctl->abort))
+            if ((given || j >= R) && !mbar_wait(&ctl->full[rc.s], rc.ph, ws, &ctl->abort))
                 break;
             Op::phase2(smem + (size_t)rc.s * kTileBytes, tile.tr, tile.tc, ctid, s_enc, ctl->ftab, p);
             __syncwarp();
@@ -756,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     named_bar_sync(1, kConsumers);
-    if (ctid == 0) {
+    if (!given && ctid == 0) {
         __threadfence();
         const uint32_t old = atomicAdd(&ws->departed, 1u);
         if (old == (uint32_t)G - 1) {

@@ -16,11 +16,14 @@ backward pass):
   Dgrad up     dX = dH W_up        A = dH  1x16 SR        B = W_up^T  (the 2-D transposed output, g of W_up)
   Wgrad up     dW_up = dH^T X      A = dH^T RHT + SR      B = X^T     RHT + RN
 
-Every activation or gradient is quantized once by nvfp4_quantize_dual, which
-reads it once and writes both its 1x16 row form (Fprop/Dgrad operand) and its
-Hadamard-transformed, token-contiguous form (Wgrad operand).  Every GEMM is
-nvfp4_gemm with bf16 output.  Twelve launches per step, all library kernels;
-this module only allocates buffers and strings the calls together.
+Every activation or gradient is quantized once, into both its 1x16 row form
+(Fprop/Dgrad operand) and its Hadamard-transformed, token-contiguous form
+(Wgrad operand).  The step's inputs X and dY go through nvfp4_quantize_dual
+(an amax pass, then the quantization).  H and dH are written by the step's own
+GEMMs: those run as nvfp4_gemm_amax, whose epilogue also reduces both tensor
+amaxes of its output, and nvfp4_quantize_dual_from_amax then quantizes them in
+one read.  Every GEMM has bf16 output.  Twelve launches per step, all library
+kernels; this module only allocates buffers and strings the calls together.
 
 Seeds: the Hadamard sign diagonal uses ``seed + 1`` for every Wgrad operand (so
 that the transforms cancel in dY^T X); stochastic rounding of dY uses
@@ -37,7 +40,7 @@ import nvfp4_bit_quantized_quantize_gb300 as nv
 
 @dataclass(frozen=True)
 class Launch:
-    kind: str          # "quantize_dual", "quantize_2d_t" or "gemm"
+    kind: str          # "quantize_dual", "quantize_dual_from_amax", "quantize_2d_t" or "gemm"
     shape: tuple       # (mode, rows, cols) for quantizers, (M, N, K) for GEMMs
     label: str         # which pass / tensor
     fn: Callable[[], None]
@@ -88,6 +91,8 @@ class MlpStep:
         self.wdq, self.wdqT = q(D, F), q(F, D)
         self.dyq, self.dyT = q(T, D), q(D, T)
         self.dhq, self.dhT = q(T, F), q(F, T)
+        # (max |.|, max |RHT(.)|) of H and dH, from the GEMMs that write them
+        self.amax = {k: torch.zeros(2, dtype=torch.float32, device=device) for k in ("H", "dH")}
         self.ws = nv.alloc_workspace(device)
 
     # the six GEMMs: D[M, N] = ga gb sum_k A[M, K] B[N, K]
@@ -116,9 +121,15 @@ class MlpStep:
         (dy_r, dy_t), (dh_r, dh_t) = self.sr_seeds["dY"], self.sr_seeds["dH"]
 
         def dual(src, C, rows_q, t_q, mode, seed, seed_t, label):
+            sh = ("sr" if mode == nv.SR else "rn", T, C)
+            if label in self.amax:  # written by a GEMM of this step, which reduced its amaxes
+                am = self.amax[label]
+                fn = lambda: nv.nvfp4_quantize_dual_from_amax(src, T, C, C, am, mode, seed, *rows_q, rs, mode,
+                                                              seed_t, *t_q, ws, stream)
+                return Launch("quantize_dual_from_amax", sh, label, fn)
             fn = lambda: nv.nvfp4_quantize_dual(src, T, C, C, mode, seed, *rows_q, rs, mode, seed_t, *t_q, ws,
                                                 stream)
-            return Launch("quantize_dual", ("sr" if mode == nv.SR else "rn", T, C), label, fn)
+            return Launch("quantize_dual", sh, label, fn)
 
         def w2d(w, R, C, wq, wqT, label):
             fn = lambda: nv.nvfp4_quantize_2d(w, R, C, C, wq[0], wq[1], wqT[0], wqT[1], wq[2], ws, stream)
@@ -129,10 +140,13 @@ class MlpStep:
             a, b, bs = getattr(self, w.a), getattr(self, w.b), getattr(self, w.b_scale_of)
             out = self.tensor(w.out, slot)
             M, N, K = w.mnk
-            gemms[w.label] = Launch(
-                "gemm", (M, N, K), w.label,
-                (lambda a=a, b=b, bs=bs, out=out, M=M, N=N, K=K:
-                 nv.nvfp4_gemm(a[0], a[1], a[2], b[0], b[1], bs[2], M, N, K, out, N, nv.OUT_BF16, ws, stream)))
+            if w.out in self.amax:
+                fn = (lambda a=a, b=b, bs=bs, out=out, M=M, N=N, K=K, am=self.amax[w.out]:
+                      nv.nvfp4_gemm_amax(a[0], a[1], a[2], b[0], b[1], bs[2], M, N, K, out, N, rs, am, ws, stream))
+            else:
+                fn = (lambda a=a, b=b, bs=bs, out=out, M=M, N=N, K=K:
+                      nv.nvfp4_gemm(a[0], a[1], a[2], b[0], b[1], bs[2], M, N, K, out, N, nv.OUT_BF16, ws, stream))
+            gemms[w.label] = Launch("gemm", (M, N, K), w.label, fn)
         return [
             dual(x, D, self.xq, self.xT, nv.RN, 0, 0, "X"),
             w2d(wu, F, D, self.wuq, self.wuqT, "W_up"),

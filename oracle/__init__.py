@@ -72,6 +72,10 @@ def lib() -> ctypes.CDLL:
         L.or_sf_bytes.restype = ctypes.c_size_t
         L.or_sf_offset.argtypes = [i64, i64, i64]
         L.or_sf_offset.restype = ctypes.c_size_t
+        L.or_amax.argtypes = [p, i64, i64, i64, p]
+        L.or_amax.restype = ctypes.c_int
+        L.or_rht_amax.argtypes = [p, i64, i64, i64, u64, p]
+        L.or_rht_amax.restype = ctypes.c_int
         L.or_quantize.argtypes = [p, i64, i64, i64, ctypes.c_int, u64, p, p, p]
         L.or_quantize.restype = ctypes.c_int
         L.or_quantize_2d.argtypes = [p, i64, i64, i64, p, p, p, p, p]
@@ -210,6 +214,28 @@ def unswizzle_sf(sf: np.ndarray, rows: int, kblocks: int) -> np.ndarray:
 
 
 # ------------------------------------------------------------ quantizers ----
+
+def amax(x_bf16: np.ndarray) -> float:
+    """max |x| over a bf16 matrix (uint16 bits): the tensor amax."""
+    x = _c(x_bf16, np.uint16)
+    R, C = x.shape
+    out = np.zeros(1, np.float32)
+    st = lib().or_amax(_ptr(x), R, C, C, _ptr(out))
+    if st != OK:
+        raise OracleError(st)
+    return float(out[0])
+
+
+def rht_amax(x_bf16: np.ndarray, rht_seed: int) -> float:
+    """max |y| over the 16-token Hadamard transforms of every channel of x [T, C]."""
+    x = _c(x_bf16, np.uint16)
+    T, C = x.shape
+    out = np.zeros(1, np.float32)
+    st = lib().or_rht_amax(_ptr(x), T, C, C, rht_seed, _ptr(out))
+    if st != OK:
+        raise OracleError(st)
+    return float(out[0])
+
 
 def quantize(x_bf16: np.ndarray, mode: int = RN, seed: int = 0):
     """1x16 quantization of a row-major bf16 matrix (given as uint16 bits)."""

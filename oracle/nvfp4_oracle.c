@@ -31,7 +31,8 @@
  * fast-math.  The matmul accumulates in binary64.
  *
  * Parity status per function: every function here is pinned by the CPU
- * tests -- e2m1/e4m3 codecs, quantizers (1x16, 2-D, RHT), stochastic
+ * tests -- e2m1/e4m3 codecs, tensor amaxes (plain and Hadamard), quantizers
+ * (1x16, 2-D, RHT), stochastic
  * rounding, scale layout, GEMM, noise meter, MXFP4 quantizer and GEMM by
  * tables from the pages, closed forms, invariants, brute force and
  * hand-worked examples; philox4x32_10 by the known-answer vectors published
@@ -349,6 +350,52 @@ static void put_code(uint8_t* q, int64_t row_bytes, int64_t r, int64_t c, int co
         *p = (uint8_t)((*p & 0xF0) | code);
 }
 
+/* Tensor amax: max |x| over an R x C bf16 matrix (leading dimension ld), the
+ * quantity the tensor scale is made from [P3 "Come funziona NVFP4?":
+ * multi-level scaling].  A non-finite element is an error. */
+int or_amax(const uint16_t* x, int64_t R, int64_t C, int64_t ld, float* amax_out)
+{
+    float amax = 0.0f;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            float a = fabsf(bf16_to_f32(x[r * ld + c]));
+            if (!(a <= FLT_MAX))
+                return OR_ERR_NONFINITE;
+            if (a > amax)
+                amax = a;
+        }
+    *amax_out = amax;
+    return OR_OK;
+}
+
+/* Tensor amax of the Hadamard form: max |y| over y = (1/4) H16 D v for every
+ * channel c and 16-token chunk v of x [T, C] [P1 "Metodología": random
+ * Hadamard transforms; the tensor scale of the transformed operand uses the
+ * transformed values].  T % 16 == 0; a non-finite y is an error. */
+int or_rht_amax(const uint16_t* x, int64_t T, int64_t C, int64_t ld, uint64_t rht_seed, float* amax_out)
+{
+    if (T % 16 != 0 || T < 0 || C < 0)
+        return OR_ERR_SHAPE;
+    const uint32_t signs = or_rht_signs(rht_seed);
+    float amax = 0.0f;
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t kb = 0; kb < T / 16; ++kb) {
+            float v[16], y[16];
+            for (int i = 0; i < 16; ++i)
+                v[i] = bf16_to_f32(x[(kb * 16 + i) * ld + c]);
+            or_rht16(v, signs, y);
+            for (int i = 0; i < 16; ++i) {
+                float a = fabsf(y[i]);
+                if (!(a <= FLT_MAX))
+                    return OR_ERR_NONFINITE;
+                if (a > amax)
+                    amax = a;
+            }
+        }
+    *amax_out = amax;
+    return OR_OK;
+}
+
 /* 1x16 quantization along rows (the contiguous axis) [P1 "Características":
  * each block of 16 contiguous elements shares an E4M3 scale].
  * x: bf16 bits, R x C with leading dimension ld.  Outputs: q (R x C/2 bytes,
@@ -361,14 +408,9 @@ int or_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int mode, u
         return OR_ERR_SHAPE;
     const int64_t KB = C / 16;
     float amax = 0.0f;
-    for (int64_t r = 0; r < R; ++r)
-        for (int64_t c = 0; c < C; ++c) {
-            float a = fabsf(bf16_to_f32(x[r * ld + c]));
-            if (!(a <= FLT_MAX))
-                return OR_ERR_NONFINITE;
-            if (a > amax)
-                amax = a;
-        }
+    int st = or_amax(x, R, C, ld, &amax);
+    if (st != OR_OK)
+        return st;
     float s_enc, gd;
     tensor_scales(amax, &s_enc, &gd);
     *g = gd;
@@ -468,20 +510,9 @@ int or_rht_quantize(const uint16_t* x, int64_t T, int64_t C, int64_t ld, uint64_
     const int64_t KB = T / 16;
     const uint32_t signs = or_rht_signs(rht_seed);
     float amax = 0.0f;
-    for (int64_t c = 0; c < C; ++c)
-        for (int64_t kb = 0; kb < KB; ++kb) {
-            float v[16], y[16];
-            for (int i = 0; i < 16; ++i)
-                v[i] = bf16_to_f32(x[(kb * 16 + i) * ld + c]);
-            or_rht16(v, signs, y);
-            for (int i = 0; i < 16; ++i) {
-                float a = fabsf(y[i]);
-                if (!(a <= FLT_MAX))
-                    return OR_ERR_NONFINITE;
-                if (a > amax)
-                    amax = a;
-            }
-        }
+    int st = or_rht_amax(x, T, C, ld, rht_seed, &amax);
+    if (st != OR_OK)
+        return st;
     float s_enc, gd;
     tensor_scales(amax, &s_enc, &gd);
     *g = gd;

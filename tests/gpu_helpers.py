@@ -137,3 +137,38 @@ def mx_gemm(qa, sfa, qb, sfb, M, N, K, out_f32=False, ws=None):
     assert np.isnan(out[:M, N:]).all(), "GEMM wrote past column N"
     assert np.isnan(out[M:]).all(), "GEMM wrote past row M"
     return np.ascontiguousarray(out[:M, :N]), st
+
+
+def gemm_amax(qa, sfa, ga, qb, sfb, gb, M, N, K, rht_seed, ws=None):
+    """nvfp4_gemm_amax into a NaN-filled, padded bf16 output (the padding must
+    come back untouched).  Returns (D as bf16 bits [M, N], amax[2], status)."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    ldd = ((N + 7) // 8) * 8
+    d = torch.full((M + 32, ldd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gat = torch.tensor([ga], dtype=torch.float32, device="cuda")
+    gbt = torch.tensor([gb], dtype=torch.float32, device="cuda")
+    amax = torch.full((2,), float("nan"), dtype=torch.float32, device="cuda")
+    ws = nv.alloc_workspace() if ws is None else ws
+    nv.nvfp4_gemm_amax(t(qa), t(sfa), gat, t(qb), t(sfb), gbt, M, N, K, d, ldd, rht_seed, amax, ws)
+    st = nv.nvfp4_device_status(ws)
+    out = d.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.all(out[:M, N:] == 0x7FC0), "GEMM wrote past column N"
+    assert np.all(out[M:] == 0x7FC0), "GEMM wrote past row M"
+    return np.ascontiguousarray(out[:M, :N]), amax.cpu().numpy(), st
+
+
+def quantize_dual_from_amax(x_bits, amax, mode, sr_seed, rht_seed, mode_t, sr_seed_t, ld=None, ws=None):
+    """nvfp4_quantize_dual_from_amax with the two maxima given as host floats."""
+    T, C = x_bits.shape
+    x = dev_bf16(x_bits, ld)
+    q, sf, g = nv.alloc_quantized(T, C)
+    qT, sfT, gT = nv.alloc_quantized(C, T)
+    for t in (q, sf, qT, sfT):
+        t.fill_(0xEE)
+    am = torch.tensor(np.asarray(amax, np.float32), device="cuda")
+    ws = nv.alloc_workspace() if ws is None else ws
+    nv.nvfp4_quantize_dual_from_amax(x, T, C, x.shape[1], am, mode, sr_seed, q, sf, g, rht_seed, mode_t,
+                                     sr_seed_t, qT, sfT, gT, ws)
+    st = nv.nvfp4_device_status(ws)
+    return (q.cpu().numpy(), sf.cpu().numpy(), float(g.cpu()[0]),
+            qT.cpu().numpy(), sfT.cpu().numpy(), float(gT.cpu()[0]), st)

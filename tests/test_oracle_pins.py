@@ -477,6 +477,50 @@ def test_nonfinite_is_an_error():
         O.quantize(x)
 
 
+def test_amax_is_the_largest_magnitude():
+    # max |x| by hand: the extreme is negative, in the last row and column
+    x = synth.f32_to_bf16_bits(np.array([[0.5, -1.0, 2.0], [0.0, 3.0, -7.5]], np.float32))
+    assert O.amax(x) == 7.5
+    assert O.amax(np.zeros((2, 16), np.uint16)) == 0.0
+    x[1, 2] = 0x7F80  # +Inf
+    with pytest.raises(O.OracleError) as e:
+        O.amax(x)
+    assert e.value.status == O.ERR_NONFINITE
+
+
+def test_amax_sets_the_quantizers_tensor_scale():
+    # g = rn(amax / 2688) with the amax the quantizers use
+    x = synth.normal_bf16((64, 48), 3, 0, 1.0, 0.0, 0.01, 50.0)
+    assert O.quantize(x)[2] == float(np.float32(np.float32(O.amax(x)) / np.float32(2688.0)))
+    for seed in (1, 9):
+        assert O.rht_quantize(x, seed)[2] == float(np.float32(np.float32(O.rht_amax(x, seed)) / np.float32(2688.0)))
+
+
+def test_rht_amax_one_hot_columns():
+    # one non-zero token v_i per 16-token chunk: every output of (1/4) H16 D v
+    # has magnitude |v_i| / 4 whatever the signs
+    x = np.zeros((32, 3), np.float32)
+    x[5, 0], x[17, 1], x[31, 2] = -12.0, 3.0, 0.5
+    xb = synth.f32_to_bf16_bits(x)
+    for seed in range(5):
+        assert O.rht_amax(xb, seed) == 3.0
+
+
+def test_rht_amax_dense_matrix_form():
+    # the transform as the dense product (1/4) H16 D v in binary64 (Sylvester
+    # H16, D from the seed's sign bits): the butterflies' binary32 roundings
+    # stay within 2^-20 of the largest input magnitude per block
+    H = _sylvester(16)
+    for seed in (0, 2, 77):
+        x = synth.normal_bf16((48, 5), seed, 4, 1.0)
+        v = synth.bf16_bits_to_f32(x).astype(np.float64)
+        s = O.rht_signs(seed)
+        D = np.array([-1.0 if (s >> i) & 1 else 1.0 for i in range(16)])
+        y = np.concatenate([0.25 * (H @ (D * v[16 * k:16 * k + 16, c])) for k in range(3) for c in range(5)])
+        got = O.rht_amax(x, seed)
+        assert abs(got - np.abs(y).max()) <= 2.0 ** -20 * np.abs(v).max() * 16
+
+
 def test_single_outlier_block_scales():
     # A single outlier sets amax; its block scale is 448 and it maps to +-6.
     x = np.zeros((4, 64), np.float32)
