@@ -94,6 +94,9 @@ class MlpStep:
         # (max |.|, max |RHT(.)|) of H and dH, from the GEMMs that write them
         self.amax = {k: torch.zeros(2, dtype=torch.float32, device=device) for k in ("H", "dH")}
         self.ws = nv.alloc_workspace(device)
+        self.ws_side = nv.alloc_workspace(device)  # for launches on a second stream
+        self._side = None
+        self._plans = {}
 
     # the six GEMMs: D[M, N] = ga gb sum_k A[M, K] B[N, K]
     def wiring(self):
@@ -114,10 +117,10 @@ class MlpStep:
             return self.outputs[slot][name]
         return getattr(self, name)
 
-    def launches(self, slot: int = 0, stream=None) -> list:
+    def launches(self, slot: int = 0, stream=None, ws=None) -> list:
         T, D, F = self.T, self.D, self.F
         x, wu, wd, dy = (self.inputs[slot][k] for k in self.IN)
-        ws, rs = self.ws, self.rht_seed
+        ws, rs = (self.ws if ws is None else ws), self.rht_seed
         (dy_r, dy_t), (dh_r, dh_t) = self.sr_seeds["dY"], self.sr_seeds["dH"]
 
         def dual(src, C, rows_q, t_q, mode, seed, seed_t, label):
@@ -163,5 +166,49 @@ class MlpStep:
         ]
 
     def run(self, slot: int = 0, stream=None) -> None:
+        """The twelve launches in order on one stream."""
         for l in self.launches(slot, stream):
             l.fn()
+
+    def run_overlapped(self, slot: int = 0, stream=None, side=None) -> None:
+        """The same launches with each weight-gradient GEMM on a second stream,
+        beside the data-gradient work that does not depend on it: dW_down =
+        dY^T H runs beside dH = dY W_down and dH's quantization, dW_up = dH^T X
+        beside dX = dH W_up.  The four GEMMs are persistent kernels with no
+        grid-wide barrier, so the second one's CTAs take the SMs the first
+        one's last, partial wave of tiles leaves idle.  The cooperative
+        quantizers (which wait on a grid-wide barrier) never overlap anything:
+        the side stream forks after them and joins before the step ends.  The
+        side GEMMs use their own workspace (self.ws_side)."""
+        import torch
+
+        main = stream if stream is not None else torch.cuda.current_stream()
+        side = side if side is not None else self.side_stream()
+        key = (slot, main, side)
+        if key not in self._plans:
+            self._plans[key] = ({l.label: l for l in self.launches(slot, main)},
+                                {l.label: l for l in self.launches(slot, side, ws=self.ws_side)})
+        ls, wg = self._plans[key]
+        for name in ("X", "W_up", "fprop_up", "H", "W_down", "fprop_down", "dY"):
+            ls[name].fn()
+        fork_a = torch.cuda.Event()
+        fork_a.record(main)
+        ls["dgrad_down"].fn()
+        side.wait_event(fork_a)          # dY's and H's Hadamard forms are ready
+        wg["wgrad_down"].fn()
+        ls["dH"].fn()
+        fork_b = torch.cuda.Event()
+        fork_b.record(main)
+        ls["dgrad_up"].fn()
+        side.wait_event(fork_b)          # dH's Hadamard form is ready
+        wg["wgrad_up"].fn()
+        join = torch.cuda.Event()
+        join.record(side)
+        main.wait_event(join)
+
+    def side_stream(self):
+        import torch
+
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=self.device)
+        return self._side

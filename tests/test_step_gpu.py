@@ -161,3 +161,20 @@ def test_step_wiring_full_shape_sampled():
         err = np.abs(got - ref)
         bound = 1e-5 * dabs + 2.0 ** -8 * np.abs(ref)
         assert np.all(err <= bound), (label, float(np.max(err - bound)))
+
+
+def test_overlapped_schedule_writes_the_same_results():
+    # the weight-gradient GEMMs on a second stream: every output and
+    # intermediate bit-identical to the one-stream order, both workspaces clean
+    T, D, F = 512, 256, 768
+    st, host = _run(T, D, F, seed=6)
+    names = ["H", "dH", "Y", "dX", "dW_up", "dW_down"]
+    seq = {n: _bits(st.tensor(n)).copy() for n in names}
+    for n in names:
+        st.tensor(n).zero_()
+    side = torch.cuda.Stream()
+    st.run_overlapped(0, torch.cuda.current_stream(), side)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_device_status(st.ws) == 0 and nv.nvfp4_device_status(st.ws_side) == 0
+    for n in names:
+        assert np.array_equal(_bits(st.tensor(n)), seq[n]), n
