@@ -830,10 +830,12 @@ def run_case(argv):
     """One library kernel on synthetic device data, for profiler captures:
 
       --case gemm M N K [f32]      random codes, E4M3 scales in [2^-6, 2^2)
+      --case gemm_amax M N K       the same, bf16 output and its two maxima
       --case quantize ROWS COLS rn|sr
       --case quantize_2d ROWS COLS
       --case rht T C rn|sr
       --case dual T C rn|sr
+      --case dual_amax T C rn|sr   the dual quantizer with both amaxes given
       --case noise ROWS COLS
 
     Two warm-up launches, then --steps launches; prints the mean CUDA-event
@@ -848,18 +850,22 @@ def run_case(argv):
     reps = CASE_REPS[0]
     torch.manual_seed(0)
     ws = nv.alloc_workspace()
-    if kind == "gemm":
+    if kind in ("gemm", "gemm_amax"):
         M, N, K = (int(v) for v in rest[:3])
-        f32 = len(rest) > 3 and rest[3] == "f32"
+        f32 = kind == "gemm" and len(rest) > 3 and rest[3] == "f32"
         a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device="cuda")
         b = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda")
         sfa = torch.randint(0x18, 0x48, (nv.nvfp4_sf_bytes(M, K),), dtype=torch.uint8, device="cuda")
         sfb = torch.randint(0x18, 0x48, (nv.nvfp4_sf_bytes(N, K),), dtype=torch.uint8, device="cuda")
         one = torch.ones(1, device="cuda")
         d = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device="cuda")
-        fn = lambda: nv.nvfp4_gemm(a, sfa, one, b, sfb, one, M, N, K, d, N, nv.OUT_F32 if f32 else nv.OUT_BF16,
-                                   ws)
-        what = f"gemm {M}x{N}x{K}{' f32' if f32 else ''}"
+        if kind == "gemm":
+            fn = lambda: nv.nvfp4_gemm(a, sfa, one, b, sfb, one, M, N, K, d, N,
+                                       nv.OUT_F32 if f32 else nv.OUT_BF16, ws)
+        else:
+            am = torch.zeros(2, dtype=torch.float32, device="cuda")
+            fn = lambda: nv.nvfp4_gemm_amax(a, sfa, one, b, sfb, one, M, N, K, d, N, 5, am, ws)
+        what = f"{kind} {M}x{N}x{K}{' f32' if f32 else ''}"
         work = lambda ms: f"{2 * M * N * K / ms / 1e9:.1f} TFLOP/s"
     else:
         R, C = int(rest[0]), int(rest[1])
@@ -879,6 +885,12 @@ def run_case(argv):
             q, sf, g = nv.alloc_quantized(R, C)
             qT, sfT, gT = nv.alloc_quantized(C, R)
             fn = lambda: nv.nvfp4_quantize_dual(x, R, C, C, mode, 1, q, sf, g, 5, mode, 2, qT, sfT, gT, ws)
+        elif kind == "dual_amax":
+            q, sf, g = nv.alloc_quantized(R, C)
+            qT, sfT, gT = nv.alloc_quantized(C, R)
+            am = torch.tensor([4.5, 4.0], dtype=torch.float32, device="cuda")  # about the maxima of N(0,1)
+            fn = lambda: nv.nvfp4_quantize_dual_from_amax(x, R, C, C, am, mode, 1, q, sf, g, 5, mode, 2, qT, sfT,
+                                                          gT, ws)
         elif kind == "noise":
             q, sf, g = nv.alloc_quantized(R, C)
             nv.nvfp4_quantize(x, R, C, C, nv.RN, 0, q, sf, g, ws)
@@ -889,7 +901,7 @@ def run_case(argv):
         what = f"{kind} {R}x{C}{' sr' if mode == nv.SR else ''}"
         byts = 2.5625 * R * C if kind == "noise" else quant_bytes(
             {"quantize": "quantize_1x16", "quantize_2d": "quantize_2d_t", "rht": "rht_quantize",
-             "dual": "quantize_dual"}[kind], R, C)
+             "dual": "quantize_dual", "dual_amax": "quantize_dual_from_amax"}[kind], R, C)
         work = lambda ms: f"{byts / ms / 1e6:.1f} GB/s algorithmic"
     stream = torch.cuda.current_stream()
     ms = _event_ms(fn, stream, reps=reps, warmup=2)
