@@ -21,7 +21,9 @@
 //            "Características del Formato NVFP4").
 //   Op2d   — same tile, one scale per 16x16 tile, optional transposed
 //            outputs ("Entrenamiento ...", "Metodología de Entrenamiento":
-//            two-dimensional block scaling for weights).
+//            two-dimensional block scaling for weights); the transposed
+//            codes and scales of a tile are staged in shared memory and leave
+//            as whole rows (a 16 KB staging area takes one tile of the ring).
 //   OpRht  — 64 tokens x 256 channels, 16-point random Hadamard transform
 //            along tokens, quantized along tokens and written channel-major
 //            ("Metodología de Entrenamiento": random Hadamard transforms);
@@ -29,9 +31,10 @@
 //            a packed binary32 operation on the pair.
 //   OpDual — the 1x16 and the Hadamard outputs of one tensor from one read,
 //            each with its own tensor scale (two amaxes reduced in phase 1).
-// The ring holds 224 KB: 14 tiles of 16 KB (1x16, 2-D) or 7 of 32 KB (RHT,
-// dual).  These kernels are bound by the latency of each thread's dependent
-// instruction chain (17 warps per SM, at most 96 registers per thread), not by
+// The ring holds 224 KB: 14 tiles of 16 KB (1x16; 13 and the staging area
+// for 2-D) or 7 of 32 KB (RHT, dual).  These kernels are bound by the
+// latency of each thread's dependent instruction chain and by their
+// instruction count (17 warps per SM, at most 96 registers per thread), not by
 // memory: the loop bookkeeping is kept free of divisions, maxima are trees,
 // and the per-call constants (Philox round keys, sign-diagonal masks) are
 // kernel parameters the host computes.
@@ -60,6 +63,18 @@ struct SmemCtl {
 };
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kRingBytes + sizeof(SmemCtl);
+
+// A barrier of `n` threads (named barrier `id`) that also returns whether
+// `v` held in every one of them.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n, bool v)
+{
+    uint32_t r;
+    asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "r"(id), "r"(n)
+                 : "memory");
+    return r != 0;
+}
 
 // Swizzled (128-byte) address of 16-byte chunk `c` of row `r` in a tile whose
 // rows are 128 bytes.
@@ -164,6 +179,7 @@ __device__ __forceinline__ uint32_t scan_tile_bf16(const uint8_t* tile, int ctid
 // the 4 blocks of a row sit in lanes 4i..4i+3 of one warp.
 struct Op1x16 {
     static constexpr int kTileBytes = 16384;
+    static constexpr int kStagingBytes = 0;  // outputs go straight to global memory
 
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tr, int32_t tc,
                                  const QuantParams&)
@@ -177,7 +193,7 @@ struct Op1x16 {
     }
 
     __device__ static void phase2(const uint8_t* tile, int32_t tr, int32_t tc, int ctid, const float (&s_enc)[2],
-                                  const float (*ftab)[128], const QuantParams& p)
+                                  const float (*ftab)[128], const QuantParams& p, uint8_t*)
     {
         const int lane = ctid & 31;
         const uint32_t row = (uint32_t)ctid >> 2, blk = ctid & 3;
@@ -234,6 +250,58 @@ __device__ __forceinline__ uint64_t nibble_transpose16(uint64_t w, int i)
 // 2w + 1 of the 32 tiles (8 row groups x 4 column blocks); lane i has row i.
 struct Op2d {
     static constexpr int kTileBytes = 16384;
+    // the transposed outputs of a tile pass through shared memory (two
+    // buffers, one per tile in flight): codes 64 rows x 64 bytes at an
+    // 80-byte row pitch, then the 64 x 8 scale bytes
+    static constexpr int kStageCodesPitch = 80;
+    static constexpr int kStageScales = 64 * kStageCodesPitch;
+    static constexpr int kStageHalf = kStageScales + 64 * 8;
+    static constexpr int kStagingBytes = 16384;
+    static_assert(2 * kStageHalf <= kStagingBytes, "staging");
+
+    // Whole 64-byte rows of the transposed codes (4 threads per row, 16 or 8
+    // bytes each) and 32-bit words of the transposed scale bytes (one per row
+    // and 4-block group), after every consumer thread has staged its part.
+    __device__ static void flush(const uint8_t* stage, int32_t tr, int32_t tc, int ctid, const QuantParams& p)
+    {
+        if (p.qT == nullptr)
+            return;
+        const int64_t kblocksT = p.rows / 16;
+        const int64_t cpT = (kblocksT + 3) / 4;
+        if (ctid < 256) {
+            const uint32_t rTl = (uint32_t)ctid >> 2, part = (uint32_t)ctid & 3u;
+            const int64_t rT = (int64_t)tc * 64 + rTl;
+            const int64_t kb0 = (int64_t)tr * 8 + part * 2;  // the first of this thread's two 16-blocks
+            if (rT < p.cols && kb0 < kblocksT) {
+                const uint4 v = *reinterpret_cast<const uint4*>(stage + rTl * kStageCodesPitch + part * 16);
+                uint8_t* dst = p.qT + rT * (p.rows / 2) + kb0 * 8;
+                const bool both = kb0 + 1 < kblocksT;
+                if (both && (p.rows & 31) == 0) {
+                    *reinterpret_cast<uint4*>(dst) = v;
+                } else {
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(v.x, v.y);
+                    if (both)
+                        *reinterpret_cast<uint2*>(dst + 8) = make_uint2(v.z, v.w);
+                }
+            }
+        } else if (ctid < 384) {
+            const uint32_t t = (uint32_t)ctid - 256u, rTl = t >> 1, grp = t & 1u;
+            const int64_t rT = (int64_t)tc * 64 + rTl;
+            const int64_t kg = (int64_t)tr * 2 + grp;  // 4-block group of the transposed matrix
+            if (kg < cpT) {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(stage + kStageScales + rTl * 8 + grp * 4);
+                *reinterpret_cast<uint32_t*>(p.sfT + ((rT >> 7) * cpT + kg) * 512 + (rT & 31) * 16 +
+                                             ((rT & 127) >> 5) * 4) = w;
+                // an odd count of 64-column tiles leaves the upper half of
+                // the last 128-row scale atom to padding: write its zeros
+                if ((p.tiles_c & 1) && tc == p.tiles_c - 1) {
+                    const int64_t rP = rT + 64;
+                    *reinterpret_cast<uint32_t*>(p.sfT + ((rP >> 7) * cpT + kg) * 512 + (rP & 31) * 16 +
+                                                 ((rP & 127) >> 5) * 4) = 0u;
+                }
+            }
+        }
+    }
 
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tr, int32_t tc,
                                  const QuantParams& p)
@@ -247,11 +315,9 @@ struct Op2d {
     }
 
     __device__ static void phase2(const uint8_t* tile, int32_t tr, int32_t tc, int ctid, const float (&s_enc)[2],
-                                  const float (*ftab)[128], const QuantParams& p)
+                                  const float (*ftab)[128], const QuantParams& p, uint8_t* stage)
     {
         const int lane = ctid & 31, cw = ctid >> 5;
-        const int64_t kblocksT = p.rows / 16;
-        const int64_t cpT = (kblocksT + 3) / 4;
         const int P = cw * 2 + (lane >> 4);
         const uint32_t g = P >> 2, blk = P & 3, i = lane & 15;
         const uint32_t row = g * 16 + i;
@@ -277,23 +343,13 @@ struct Op2d {
             *reinterpret_cast<uint2*>(p.q + grow * (p.cols / 2) + gcol / 2) = make_uint2(lo32, hi32);
         p.sf[((int64_t)tr * p.tiles_c + tc) * 512 + (row & 31) * 16 + (row >> 5) * 4 + blk] = (uint8_t)sb;
         if (p.qT != nullptr) {
+            // column blk * 16 + i of the tile: its 8 bytes of codes (16-block g
+            // of that transposed row) and the tile's scale byte, staged
             const uint64_t col = nibble_transpose16(((uint64_t)hi32 << 32) | lo32, (int)i);
-            const int64_t rT = gcol + i;     // row of the transposed matrix
-            const int64_t kbT = (int64_t)tr * 8 + g;  // its 16-block index
-            if (rT < p.cols && kbT < kblocksT)
-                *reinterpret_cast<uint2*>(p.qT + rT * (p.rows / 2) + kbT * 8) =
-                    make_uint2((uint32_t)col, (uint32_t)(col >> 32));
-            if (kbT < 4 * cpT) {
-                p.sfT[((rT >> 7) * cpT + (kbT >> 2)) * 512 + (rT & 31) * 16 + ((rT & 127) >> 5) * 4 + (kbT & 3)] =
-                    (uint8_t)sb;
-                // an odd count of 64-column tiles leaves the upper half of
-                // the last 128-row scale atom to padding: write its zeros
-                if ((p.tiles_c & 1) && tc == p.tiles_c - 1) {
-                    const int64_t rP = rT + 64;
-                    p.sfT[((rP >> 7) * cpT + (kbT >> 2)) * 512 + (rP & 31) * 16 + ((rP & 127) >> 5) * 4 +
-                          (kbT & 3)] = 0;
-                }
-            }
+            const uint32_t rTl = blk * 16 + i;
+            *reinterpret_cast<uint2*>(stage + rTl * kStageCodesPitch + g * 8) =
+                make_uint2((uint32_t)col, (uint32_t)(col >> 32));
+            stage[kStageScales + rTl * 8 + g] = (uint8_t)sb;
         }
     }
 };
@@ -307,6 +363,7 @@ struct Op2d {
 // packed binary32 operation for the two channels.
 struct OpRht {
     static constexpr int kTileBytes = 32768;
+    static constexpr int kStagingBytes = 0;  // outputs go straight to global memory
 
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tt, int32_t ct,
                                  const QuantParams&)
@@ -452,7 +509,7 @@ struct OpRht {
     }
 
     __device__ static void phase2(const uint8_t* tile, int32_t tt, int32_t ct, int ctid, const float (&s_enc)[2],
-                                  const float (*ftab)[128], const QuantParams& p)
+                                  const float (*ftab)[128], const QuantParams& p, uint8_t*)
     {
         quantize_out(tile, tt, ct, ctid, s_enc[0], ftab[0], p.mode, p.keys[0], p.q, p.sf, p);
     }
@@ -468,6 +525,7 @@ struct OpRht {
 // OpRht's channel pair.
 struct OpDual {
     static constexpr int kTileBytes = OpRht::kTileBytes;
+    static constexpr int kStagingBytes = 0;  // outputs go straight to global memory
 
     __device__ static void issue(const CUtensorMap* m, uint8_t* dst, uint64_t* bar, int32_t tt, int32_t ct,
                                  const QuantParams& p)
@@ -542,7 +600,7 @@ struct OpDual {
     }
 
     __device__ static void phase2(const uint8_t* tile, int32_t tt, int32_t ct, int ctid, const float (&s_enc)[2],
-                                  const float (*ftab)[128], const QuantParams& p)
+                                  const float (*ftab)[128], const QuantParams& p, uint8_t*)
     {
         const int lane = ctid & 31;
         uint32_t row, box0, blk;
@@ -610,12 +668,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                           Workspace* ws)
 {
     constexpr int kTileBytes = Op::kTileBytes;
-    constexpr int kStages = kRingBytes / kTileBytes;
+    constexpr int kStages = (kRingBytes - Op::kStagingBytes) / kTileBytes;
     static_assert(kStages <= kMaxStages, "ring");
     using Ring = RingCursor<kStages>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (size_t)kRingBytes);
+    uint8_t* staging = smem + (size_t)(kRingBytes - Op::kStagingBytes);  // (ops that stage outputs)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t G = gridDim.x, bid = blockIdx.x;
@@ -761,9 +820,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t j = 0; j < n; ++j, rc.next()) {
             if (j == R)  // then the re-loads, from tile t_begin + n - R - 1 down
                 tile.set(t_begin + n - R - 1, tiles_c);
-            if ((given || j >= R) && !mbar_wait(&ctl->full[rc.s], rc.ph, ws, &ctl->abort))
-                break;
-            Op::phase2(smem + (size_t)rc.s * kTileBytes, tile.tr, tile.tc, ctid, s_enc, ctl->ftab, p);
+            const bool ok = !(given || j >= R) || mbar_wait(&ctl->full[rc.s], rc.ph, ws, &ctl->abort);
+            uint8_t* stage = staging + (j & 1u) * (Op::kStagingBytes / 2);
+            if constexpr (Op::kStagingBytes > 0) {
+                // every consumer thread reaches this barrier on every tile (its
+                // waits are bounded), so a failed wait ends the loop for all
+                // of them at once; past it the staged tile is complete, and the
+                // other buffer's tile was flushed before it
+                if (ok)
+                    Op::phase2(smem + (size_t)rc.s * kTileBytes, tile.tr, tile.tc, ctid, s_enc, ctl->ftab, p, stage);
+                if (!named_bar_and(1, kConsumers, ok))
+                    break;
+                Op::flush(stage, tile.tr, tile.tc, ctid, p);
+            } else {
+                if (!ok)
+                    break;
+                Op::phase2(smem + (size_t)rc.s * kTileBytes, tile.tr, tile.tc, ctid, s_enc, ctl->ftab, p, stage);
+            }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&ctl->empty[rc.s]);
