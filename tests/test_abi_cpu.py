@@ -88,6 +88,20 @@ def test_host_validation_rejects_before_launch(lib):
                                  None) == 1
     assert L.nvfp4_quantize_dual(fake, 32, 32, 32, 0, 0, fake, fake, fake, 1, 1, 0, None, fake, fake, fake,
                                  None) == 1
+    # GEMM with output maxima: M % 16, N % 16, an amax buffer, bf16 output rows of 16-byte multiples
+    assert L.nvfp4_gemm_amax(fake, fake, fake, fake, fake, fake, 24, 32, 64, fake, 32, 0, fake, fake, None) == 2
+    assert L.nvfp4_gemm_amax(fake, fake, fake, fake, fake, fake, 32, 40, 64, fake, 40, 0, fake, fake, None) == 2
+    assert L.nvfp4_gemm_amax(fake, fake, fake, fake, fake, fake, 32, 32, 80, fake, 32, 0, fake, fake, None) == 2
+    assert L.nvfp4_gemm_amax(fake, fake, fake, fake, fake, fake, 32, 32, 64, fake, 32, 0, None, fake, None) == 1
+    assert L.nvfp4_gemm_amax(fake, fake, fake, fake, fake, fake, 32, 32, 64, fake, 36, 0, fake, fake, None) == 3
+    assert L.nvfp4_gemm_amax(fake, fake, fake, fake, fake, fake, 32, 32, 64, fake, 32, 0, fake + 2, fake, None) == 3
+    # one-read dual quantizer: an amax buffer (4-byte aligned), then the dual quantizer's rules
+    assert L.nvfp4_quantize_dual_from_amax(fake, 32, 32, 32, None, 0, 0, fake, fake, fake, 1, 1, 0, fake, fake,
+                                           fake, fake, None) == 1
+    assert L.nvfp4_quantize_dual_from_amax(fake, 32, 32, 32, fake + 2, 0, 0, fake, fake, fake, 1, 1, 0, fake,
+                                           fake, fake, fake, None) == 3
+    assert L.nvfp4_quantize_dual_from_amax(fake, 24, 32, 32, fake, 0, 0, fake, fake, fake, 1, 1, 0, fake, fake,
+                                           fake, fake, None) == 2
     assert L.nvfp4_workspace_init(None, None) == 1
     # noise meter: cols % 16, 8-byte aligned sums
     assert L.nvfp4_quant_noise(fake, 16, 24, 24, fake, fake, fake, fake, None) == 2
