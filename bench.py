@@ -620,6 +620,20 @@ def measure_configs(step, stream, pk):
     return out
 
 
+def cublaslt_nvfp4(a, b, M, N, K):
+    """cuBLASLt's block-scaled NVFP4 GEMM through torch._scaled_mm on codes and
+    128x4-atom scale bytes laid out as this library writes them (the layout
+    the library call reads as its swizzled block scales).  Returns the call."""
+    import torch
+
+    rup = lambda x, m: (x + m - 1) // m * m
+    A = a[0].view(torch.float4_e2m1fn_x2)
+    B = b[0].view(torch.float4_e2m1fn_x2)
+    SA = a[1].view(torch.float8_e4m3fn).view(rup(M, 128), rup(K // 16, 4))
+    SB = b[1].view(torch.float8_e4m3fn).view(rup(N, 128), rup(K // 16, 4))
+    return lambda: torch._scaled_mm(A, B.t(), SA, SB, out_dtype=torch.bfloat16)
+
+
 def measure_extras(step, stream, pk):
     """Kernels beside the step, each timed alone (not part of `value`):
     the quantization-noise meter on H's forward form, a GEMM with ragged
@@ -678,6 +692,18 @@ def measure_extras(step, stream, pk):
     out["mxfp4_gemm[8192x11008x4096]"] = {"ms": round(ms, 4),
                                            "TFLOP/s": round(GEMM_FLOPS / (ms * 1e-3) / 1e12, 1)}
     del mq, msf, xa, wb
+    # cuBLASLt's NVFP4 GEMM on the up-projection Fprop shape (context: the
+    # vendor library on the same operands' codes and block scales)
+    key = "cublaslt_nvfp4[8192x11008x4096]"
+    try:
+        fn = cublaslt_nvfp4(step.xq[:2], step.wuq[:2], T, F, D)
+        fn()
+        ms = _event_ms(fn, stream, reps=5)
+        out[key] = {"ms": round(ms, 4), "TFLOP/s": round(GEMM_FLOPS / (ms * 1e-3) / 1e12, 1),
+                    "note": "torch._scaled_mm, bf16 out, block scales only (no tensor scale); context, not this "
+                            "library"}
+    except Exception as e:  # a torch without NVFP4 _scaled_mm
+        out[key] = {"unavailable": str(e).splitlines()[0][:160]}
     # cuBLAS bf16 on the same six GEMMs (context: the unquantized layer)
     shapes = [(T, F, D), (T, D, F), (T, F, D), (D, F, T), (T, D, F), (F, D, T)]
     tot = 0.0
@@ -831,6 +857,7 @@ def run_case(argv):
 
       --case gemm M N K [f32]      random codes, E4M3 scales in [2^-6, 2^2)
       --case gemm_amax M N K       the same, bf16 output and its two maxima
+      --case cublaslt M N K        cuBLASLt's NVFP4 GEMM on the same kind of data (context)
       --case quantize ROWS COLS rn|sr
       --case quantize_2d ROWS COLS
       --case rht T C rn|sr
@@ -850,7 +877,16 @@ def run_case(argv):
     reps = CASE_REPS[0]
     torch.manual_seed(0)
     ws = nv.alloc_workspace()
-    if kind in ("gemm", "gemm_amax"):
+    if kind == "cublaslt":
+        M, N, K = (int(v) for v in rest[:3])
+        a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device="cuda")
+        b = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda")
+        sfa = torch.randint(0x18, 0x48, (nv.nvfp4_sf_bytes(M, K),), dtype=torch.uint8, device="cuda")
+        sfb = torch.randint(0x18, 0x48, (nv.nvfp4_sf_bytes(N, K),), dtype=torch.uint8, device="cuda")
+        fn = cublaslt_nvfp4((a, sfa), (b, sfb), M, N, K)
+        what = f"cublaslt {M}x{N}x{K}"
+        work = lambda ms: f"{2 * M * N * K / ms / 1e9:.1f} TFLOP/s"
+    elif kind in ("gemm", "gemm_amax"):
         M, N, K = (int(v) for v in rest[:3])
         f32 = kind == "gemm" and len(rest) > 3 and rest[3] == "f32"
         a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device="cuda")
