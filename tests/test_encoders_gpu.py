@@ -1,6 +1,6 @@
 """Device element encoders (the exact code paths the quantizers use) against
-the oracle's nearest/stochastic rounding, on every transition point of both
-formats and on random inputs."""
+the oracle's nearest/stochastic rounding: on every transition point of both
+formats and on random inputs, then on every binary32 input up to infinity."""
 import numpy as np
 import pytest
 import torch
@@ -72,3 +72,96 @@ def test_e2m1_sr_encoder_matches_oracle():
     r2 = rng.integers(0, 65536, v2.size).astype(np.uint16)
     _, _, sr2 = _probe(v2, r2)
     assert np.array_equal(sr2, O.e2m1_sr_many(v2, r2))
+
+
+# ---------------------------------------------------------------------------
+# Every binary32 input.  Each encoder below is, for a fixed random value, a
+# non-decreasing function of |x| onto consecutive codes (nearest rounding with
+# a fixed tie rule; stochastic rounding with a fixed random value, whose carry
+# point moves up with the fraction and resets to the next grid value), and for
+# non-negative binary32 the bit patterns order like the values.  So the
+# oracle's whole graph over the 2^31 non-negative patterns up to +inf is the
+# step function given by the first pattern of each code, found below by
+# bisection on the oracle; the device is then compared with that step function
+# on every pattern, and on the negative patterns (E2M1) with the sign code
+# added.  NaN is left out: the quantizers report a non-finite tensor before
+# anything reaches an encoder.
+# ---------------------------------------------------------------------------
+
+_INF = 0x7F800000
+_CHUNK = 1 << 27
+
+
+def _code_starts(fn, ncodes):
+    """First pattern in [0, +inf] at which fn (patterns -> codes, the oracle)
+    reaches each code 1..ncodes-1."""
+    target = np.arange(1, ncodes, dtype=np.int64)
+    lo = np.zeros(target.size, np.int64)
+    hi = np.full(target.size, _INF, np.int64)
+    assert np.all(fn(lo) < target) and np.all(fn(hi) >= target)
+    while np.any(hi - lo > 1):
+        mid = (lo + hi) // 2
+        up = fn(mid) >= target
+        hi, lo = np.where(up, mid, hi), np.where(up, lo, mid)
+    # consecutive codes: each start lies below the next, and the oracle just
+    # below a start gives the previous code
+    assert np.all(np.diff(hi) > 0)
+    assert np.array_equal(fn(hi - 1), target - 1) and np.array_equal(fn(hi), target)
+    return hi
+
+
+def _as_f32(patterns):
+    return np.asarray(patterns, np.int64).astype(np.uint32).view(np.float32)
+
+
+def _sweep(starts, probe, signed):
+    """Compare probe(v) with the step function on every pattern in [0, +inf],
+    and on its negation with code | 8 when signed.  Returns the number of
+    patterns checked."""
+    starts_t = torch.from_numpy(starts).cuda()
+    done = 0
+    for base in range(0, _INF + 1, _CHUNK):
+        n = min(_CHUNK, _INF + 1 - base)
+        pat = torch.arange(base, base + n, dtype=torch.int64, device="cuda")
+        want = torch.searchsorted(starts_t, pat, right=True).to(torch.uint8)
+        v = pat.to(torch.int32).view(torch.float32)
+        del pat
+        got = probe(v)
+        bad = torch.nonzero(got != want)
+        assert bad.numel() == 0, f"pattern {base + int(bad[0]):#010x}: {int(got[bad[0]])} != {int(want[bad[0]])}"
+        if signed:
+            got = probe(torch.neg(v))
+            bad = torch.nonzero(got != (want | 8))
+            assert bad.numel() == 0, f"pattern -{base + int(bad[0]):#010x}"
+        done += n * (2 if signed else 1)
+    torch.cuda.synchronize()
+    return done
+
+
+def _probe_dev(v, which, R=None):
+    n = v.numel()
+    out = torch.empty(n, dtype=torch.uint8, device="cuda")
+    r = None if R is None else torch.full((n,), R - ((R & 0x8000) << 1), dtype=torch.int16, device="cuda")
+    outs = {"e4m3": None, "rn": None, "sr": None}
+    outs[which] = out
+    nv.nvfp4_encode_probe(v, r, n, outs["e4m3"], outs["rn"], outs["sr"])
+    return out
+
+
+def test_e4m3_encoder_on_every_nonnegative_binary32():
+    starts = _code_starts(lambda p: O.e4m3_rn_sat_many(_as_f32(p)), 0x7F)
+    assert _sweep(starts, lambda v: _probe_dev(v, "e4m3"), signed=False) == _INF + 1
+
+
+def test_e2m1_rn_encoder_on_every_binary32():
+    starts = _code_starts(lambda p: O.e2m1_rn_many(_as_f32(p)), 8)
+    assert _sweep(starts, lambda v: _probe_dev(v, "rn"), signed=True) == 2 * (_INF + 1)
+
+
+@pytest.mark.parametrize("R", [0x0000, 0x0001, 0x7FFF, 0x8000, 0xA5C3, 0xFFFF])
+def test_e2m1_sr_encoder_on_every_binary32_for_one_random_value(R):
+    def oracle(p):
+        v = _as_f32(p)
+        return O.e2m1_sr_many(v, np.full(v.size, R, np.uint16))
+    starts = _code_starts(oracle, 8)
+    assert _sweep(starts, lambda v: _probe_dev(v, "sr", R), signed=True) == 2 * (_INF + 1)
