@@ -12,12 +12,10 @@
 // elements inside M x N.
 //
 // Two kernels: the paired-SM kernel at the end of this file (256 x 256 tiles
-// on two SMs, tcgen05 cta_group::2) runs every matrix of more than 128 rows;
-// the one-SM kernel here (128 x 256 tiles) runs the rest.  Both are bound by
-// shared-memory traffic per SM (tensor-copy writes, tensor-core operand
-// reads, the scale warps' reads, epilogue staging); the pair moves a third
-// less of it per flop.  In the one-SM kernel each CTA owns a persistent
-// sequence of 128 x 256 output tiles:
+// on two SMs, tcgen05 cta_group::2) runs every matrix of more than 128 rows
+// and every call that wants the output maxima; the one-SM kernel here
+// (128 x 256 tiles) runs the rest.  In the one-SM kernel each CTA owns a
+// persistent sequence of 128 x 256 output tiles:
 //   warp 0  TMA producer: A/B tiles (128-byte swizzle) and the scale atoms
 //           (3-D tensor boxes of 4 atoms) into a 4-stage shared-memory ring;
 //   warp 1  allocates tensor memory and issues tcgen05.mma.kind::mxf4nvf4
@@ -33,9 +31,11 @@
 //           atoms from shared memory into that quarter's lanes with
 //           tcgen05.st (every quarter holds the four 32-row groups of an atom,
 //           the layout the MMA reads), wait for the stores and signal the
-//           MMA warp.  A tcgen05.cp of the atoms would cost the tensor pipe
-//           about 56 cycles per copy, three copies per MMA — half the
-//           kernel's time; stores by these warps take none of it.
+//           MMA warp.  (Issued by the MMA thread's single lane, a tcgen05.cp
+//           of the atoms cost the tensor pipe ~56 cycles per copy, three per
+//           MMA; the paired kernel issues its copies under elect.sync, where
+//           they cost next to nothing.  This kernel runs only matrices of at
+//           most 128 rows and keeps the store path.)
 // The MMA warp's issue loop is kept lean: every descriptor is a precomputed
 // base plus a constant offset, the four K = 64 steps of a stage are unrolled.
 // Every wait is bounded; a wait that runs out records NVFP4_ERR_TIMEOUT and
@@ -344,48 +344,73 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================ paired SMs ====
 // The same GEMM on two SMs per output tile (tcgen05 cta_group::2): a cluster
 // of two CTAs computes a 256 x 256 tile with one M = 256, N = 256, K = 64 MMA
-// per step, issued by one thread of the even CTA.  Each CTA stages its own
-// 128 rows of A and its own 128 rows of B (the tensor cores exchange the B
-// halves), so each SM receives 38 KB per K = 256 stage (A, B and the scale
-// atoms) instead of the one-SM kernel's 54 KB for the same work, and the
-// freed shared memory holds a fifth stage.  Each CTA's tensor memory holds
-// the accumulator of its 128 A rows (256 columns) and, per stage, its A rows'
-// scale atoms and the atoms of all 256 B rows, written there by its own four
-// scale warps with tcgen05.st.
-//   warp 0     TMA producer (both CTAs): this CTA's A and B boxes, its A
-//              rows' scale atoms and both B row tiles' atoms, all on this
-//              CTA's `full` barrier;
+// per step, issued by the even CTA.  Each CTA stages its own 128 rows of A,
+// its own 128 rows of B (the tensor cores exchange the B halves), its A rows'
+// scale atoms and the atoms of all 256 B rows, so each SM receives 38 KB per
+// K = 256 stage instead of the one-SM kernel's 54 KB for the same work, and
+// the freed shared memory holds a fifth stage.  Each CTA's tensor memory holds
+// the accumulator of its 128 A rows (256 columns) and five scale slots, one
+// per ring stage.
+//   warp 0     TMA producer (both CTAs): this CTA's A and B boxes and scale
+//              atoms of each stage; the bytes of both CTAs complete on the
+//              even CTA's `full` barrier of the stage (the .cta_group::2 form
+//              of the tensor copy), which expects both;
 //   warp 1     tensor-memory allocation (collective over the pair); in the
-//              even CTA, the MMA issuer;
-//   warps 2-9  epilogue, as in the one-SM kernel;
-//   warps 10-13 scale warps: once their CTA's stage landed and the
-//              tensor-memory slot is free, tcgen05.st of the atoms, then one
-//              arrive on the even CTA's sf_ready barrier of the stage -- eight
-//              arrivals (four per CTA) say that both CTAs' stage is in place,
-//              so the MMA thread waits on that one barrier per stage.
-// Stage-free, slot-free and accumulator-full signals reach both CTAs through
-// the multicast form of tcgen05.commit; the odd CTA's scale-ready and
-// drained-accumulator signals reach the even CTA by remote mbarrier arrives
-// with the default (CTA-scope release) semantics: what they report was
-// completed by an earlier wait of the arriving thread (TMA completion,
-// tcgen05.wait::st or ::ld, then tcgen05.fence::before_thread_sync), and a
-// cluster-scope release on these arrives halved the kernel's speed.  Every
-// wait is bounded; a cluster barrier keeps both CTAs (whose shared and tensor
-// memory the MMAs use) alive until all tensor-core work is done.
+//              even CTA, the MMA warp: per stage, once `full` says that both
+//              CTAs' stage landed, one elected lane copies the scale atoms
+//              into the stage's tensor-memory slot with tcgen05.cp (in both
+//              CTAs) and issues the MMAs, three copies before each MMA, then
+//              commits the stage free to both CTAs' producers;
+//   warps 2-9  epilogue, as in the one-SM kernel.
+// The copies and MMAs of a stage go out under elect.sync from the converged
+// warp.  Issued by one lane inside a divergent branch, every copy cost the
+// tensor pipe ~40-56 cycles and the whole kernel half its speed; under
+// elect.sync they cost next to nothing.  A stage's scale slot is rewritten
+// only after the stage's next `full`, which the producer armed after the
+// MMAs that read the slot had completed.
+// Stage-free and accumulator-full signals reach both CTAs through the
+// multicast form of tcgen05.commit; the odd CTA's drained-accumulator signals
+// reach the even CTA by remote mbarrier arrives with the default (CTA-scope
+// release) semantics: what they report was completed by an earlier wait of
+// the arriving thread (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync),
+// and a cluster-scope release on these arrives halved the kernel's speed.
+// Every wait is bounded.  The MMA warp's loops always run to their end (a
+// wait that fails sets the abort flag, after which every later wait returns
+// at once and the remaining MMAs read valid, stale operands), so no branch in
+// the issuing loop depends on a wait.  A cluster barrier keeps both CTAs
+// (whose shared and tensor memory the MMAs use) alive until all tensor-core
+// work is done; after a failed wait, every CTA first gives the tensor copies
+// it may have in flight time to land.
+// One lane of the converged warp (the lowest active one).
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t p;
+    asm volatile("{\n.reg .pred q;\n.reg .b32 r;\nelect.sync r|q, 0xffffffff;\nselp.u32 %0, 1, 0, q;\n}" : "=r"(p));
+    return p != 0;
+}
+
+// One 128 x 4 scale atom (32 rows x 16 bytes of shared memory, every row
+// holding the 4 scales of rows r, r + 32, r + 64, r + 96) into 4 columns of
+// all four lane quarters of tensor memory, in both CTAs of the pair (each
+// CTA's own shared memory into its own tensor memory): the layout the
+// block-scaled MMA reads.
+__device__ __forceinline__ void tmem_cp_pair_atom(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 constexpr int PM = 256;
 constexpr int PN = 256;
 constexpr int kPA = 128 * BK / 2;              // 16 KB: this CTA's 128 rows of A
 constexpr int kPB = 128 * BK / 2;              // 16 KB: this CTA's 128 rows of B
 constexpr int kPStage = kPA + kPB + kSfaBytes + kSfbBytes;
 constexpr int kPStages = 5;                    // shared-memory ring (5 x 38 KB)
-constexpr int kPSlots = 4;                     // scale slots in tensor memory (a ring of their own)
-constexpr uint32_t kPSlotStride = 64;          // A's 4 steps x 4 columns, B's 4 steps x 8 (48 used)
+constexpr uint32_t kPSlotStride = 48;          // scale slot: A's 4 steps x 4 columns, B's 4 steps x 8
+constexpr int kPThreads = (2 + kEpilogueWarps) * 32;  // producer, MMA, epilogue (no scale warps)
 
 struct PairCtl {
-    uint64_t full[kPStages];      // this CTA's stage landed
+    uint64_t full[kPStages];      // even CTA: both CTAs' stage landed (A, B, scale atoms)
     uint64_t empty[kPStages];     // the stage's MMAs are done (multicast commit)
-    uint64_t sf_ready[kPStages];  // even CTA: both CTAs' stage landed and its scales are in tensor memory
-    uint64_t sf_free[kPSlots];    // the MMAs reading the scale slot are done (multicast commit)
     uint64_t tmem_full;
     uint64_t tmem_empty;          // even CTA: both CTAs drained the accumulator (16 arrivals)
     uint64_t drain;
@@ -395,7 +420,7 @@ struct PairCtl {
 
 constexpr size_t kPSmemBytes = 1024 + (size_t)kPStages * kPStage + kEpilogueWarps * kWideBufBytes + sizeof(PairCtl);
 static_assert(kPStage % 1024 == 0, "stage alignment");
-static_assert(kAccCols + kPSlots * kPSlotStride <= kTmemCols, "tensor memory budget");
+static_assert(kAccCols + kPStages * kPSlotStride <= kTmemCols, "tensor memory budget");
 static_assert(kPSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kStoreBufBytes + kRhtBufBytes <= kWideBufBytes, "epilogue buffer: bf16 chunk + Hadamard scratch");
 
@@ -413,7 +438,7 @@ __device__ __forceinline__ void mma_step_pair(uint32_t d, uint64_t adesc, uint64
 }
 
 template <bool kMx>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(128)
     nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                           const __grid_constant__ CUtensorMap tma_sfa, const __grid_constant__ CUtensorMap tma_sfb,
                           const __grid_constant__ CUtensorMap tma_d, const GemmArgs args, Workspace* ws)
@@ -440,10 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kPStages; ++s) {
             mbar_init(&ctl->full[s], 1);
             mbar_init(&ctl->empty[s], 1);
-            mbar_init(&ctl->sf_ready[s], 2 * kScaleWarps);
         }
-        for (int s = 0; s < kPSlots; ++s)
-            mbar_init(&ctl->sf_free[s], 1);
         mbar_init(&ctl->tmem_full, 1);
         mbar_init(&ctl->tmem_empty, 2 * kEpilogueWarps);
         mbar_init(&ctl->drain, 1);
@@ -475,60 +497,91 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tm = t % tiles_m, tn = t / tiles_m;
             const uint32_t arow = 2 * tm + rank;   // this CTA's 128-row tile of A
             uint8_t* st = smem + (size_t)s * kPStage;
-            // boxes past M, N or K read as zeros and still count in full
-            mbar_expect_tx(&ctl->full[s], kPStage);
-            tma_load_2d(st, &tma_a, &ctl->full[s], (int32_t)(ks * 128), (int32_t)(arow * 128));
-            tma_load_2d(st + kPA, &tma_b, &ctl->full[s], (int32_t)(ks * 128), (int32_t)((2 * tn + rank) * 128));
-            tma_load_3d(st + kPA + kPB, &tma_sfa, &ctl->full[s], 0, (int32_t)(ks * 4), (int32_t)arow);
-            tma_load_3d(st + kPA + kPB + kSfaBytes, &tma_sfb, &ctl->full[s], 0, (int32_t)(ks * 4),
-                        (int32_t)(2 * tn));
+            // boxes past M, N or K read as zeros and still count in full; both
+            // CTAs' bytes complete on the even CTA's barrier, armed by the even
+            // CTA for both (a byte count may arrive before the arming: the
+            // phase completes only with its one arrival and a zero count)
+            const uint32_t bar = mapa_shared(smem_u32(&ctl->full[s]), 0);
+            if (rank == 0)
+                mbar_expect_tx(&ctl->full[s], 2 * kPStage);
+            tma_load_2d_pair(st, &tma_a, bar, (int32_t)(ks * 128), (int32_t)(arow * 128));
+            tma_load_2d_pair(st + kPA, &tma_b, bar, (int32_t)(ks * 128), (int32_t)((2 * tn + rank) * 128));
+            tma_load_3d_pair(st + kPA + kPB, &tma_sfa, bar, 0, (int32_t)(ks * 4), (int32_t)arow);
+            tma_load_3d_pair(st + kPA + kPB + kSfaBytes, &tma_sfb, bar, 0, (int32_t)(ks * 4), (int32_t)(2 * tn));
         }
-        // never leave with copies in flight
-        for (uint32_t k = ia > kPStages ? ia - kPStages : 0; k < ia; ++k)
-            mbar_wait(&ctl->full[k % kPStages], (k / kPStages) & 1, ws, nullptr);
-    } else if (warp == 1 && lane == 0 && rank == 0) {
-        // ------------------------------------------------------ MMA issuer ----
+        // never leave with copies in flight: the even CTA's barriers count
+        // both CTAs' copies of the stages it armed (after a failed wait the
+        // settle below covers the rest)
+        if (rank == 0)
+            for (uint32_t k = ia > kPStages ? ia - kPStages : 0; k < ia; ++k)
+                mbar_wait(&ctl->full[k % kPStages], (k / kPStages) & 1, ws, abort);
+    } else if (warp == 1 && rank == 0) {
+        // ------------------------------------------------------- MMA warp ----
         const uint32_t base = smem_u32(smem);
         const uint64_t a_desc = smem_desc(base, 16, 1024, kSwizzle128B);
         const uint64_t b_desc = smem_desc(base + kPA, 16, 1024, kSwizzle128B);
+        // scale atoms: 512-byte blocks of 32 rows x 16 bytes, no swizzle
+        const uint64_t sf_desc = smem_desc(base + kPA + kPB, 0, 128, 0);
         constexpr uint32_t kStageDesc = kPStage >> 4;  // stage stride in descriptor units
+        constexpr uint32_t kSfbDesc = kSfaBytes >> 4;  // B's atoms after A's
+        constexpr uint32_t kAtomDesc = 512 >> 4;
         constexpr uint16_t kBoth = 0x3;
         uint32_t i = 0;
-        for (uint32_t n = 0; n < my_tiles && !*abort; ++n) {
-            if (n > 0 && !mbar_wait(&ctl->tmem_empty, (n - 1) & 1, ws, abort))
-                break;
+        for (uint32_t n = 0; n < my_tiles; ++n) {
+            if (n > 0) {
+                if (lane == 0)
+                    mbar_wait(&ctl->tmem_empty, (n - 1) & 1, ws, abort);
+                __syncwarp();
+            }
             tc_fence_after();
             for (uint32_t ks = 0; ks < kstages; ++ks, ++i) {
-                const uint32_t s = i % kPStages, u = i % kPSlots;
-                // both CTAs' scale warps saw their stage land and wrote its
-                // scale atoms before they signalled
-                if (!mbar_wait(&ctl->sf_ready[s], (i / kPStages) & 1, ws, abort))
-                    goto mma_done;
+                const uint32_t s = i % kPStages;
+                if (lane == 0)
+                    mbar_wait(&ctl->full[s], (i / kPStages) & 1, ws, abort);
+                __syncwarp();
                 tc_fence_after();
                 const uint64_t off = (uint64_t)(s * kStageDesc);
-                const uint32_t sfa_t = tmem + kAccCols + u * kPSlotStride;
+                const uint64_t sfa_src = sf_desc + off, sfb_src = sfa_src + kSfbDesc;
+                const uint32_t sfa_t = tmem + kAccCols + s * kPSlotStride;
                 const uint32_t sfb_t = sfa_t + 16;
                 const uint32_t k_left = (uint32_t)args.K - ks * BK;
-                if (k_left >= BK) {
+                const uint32_t kk = k_left >= BK ? 4u : (k_left + 63) / 64;
+                if (elect_one()) {
+                    // K step j: A's atom j into columns 4j, B's row tiles' atoms
+                    // j (rows 0-127) and 4 + j (rows 128-255) into 8j and 8j + 4
+                    if (kk == 4) {
 #pragma unroll
-                    for (uint32_t j = 0; j < 4; ++j)
-                        mma_step_pair<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
-                                           sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
-                } else {
-                    const uint32_t kk = (k_left + 63) / 64;
-                    for (uint32_t j = 0; j < kk; ++j)
-                        mma_step_pair<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
-                                           sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                        for (uint32_t j = 0; j < 4; ++j) {
+                            tmem_cp_pair_atom(sfa_t + 4 * j, sfa_src + kAtomDesc * j);
+                            tmem_cp_pair_atom(sfb_t + 8 * j, sfb_src + kAtomDesc * j);
+                            tmem_cp_pair_atom(sfb_t + 8 * j + 4, sfb_src + kAtomDesc * (4 + j));
+                            mma_step_pair<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
+                                               sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                        }
+                    } else {
+                        for (uint32_t j = 0; j < kk; ++j) {
+                            tmem_cp_pair_atom(sfa_t + 4 * j, sfa_src + kAtomDesc * j);
+                            tmem_cp_pair_atom(sfb_t + 8 * j, sfb_src + kAtomDesc * j);
+                            tmem_cp_pair_atom(sfb_t + 8 * j + 4, sfb_src + kAtomDesc * (4 + j));
+                            mma_step_pair<kMx>(tmem, a_desc + off + 2 * j, b_desc + off + 2 * j, sfa_t + 4 * j,
+                                               sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                        }
+                    }
+                    tc_commit_pair_multicast(&ctl->empty[s], kBoth);
                 }
-                tc_commit_pair_multicast(&ctl->empty[s], kBoth);
-                tc_commit_pair_multicast(&ctl->sf_free[u], kBoth);
+                __syncwarp();
             }
-            tc_commit_pair_multicast(&ctl->tmem_full, kBoth);
+            if (elect_one())
+                tc_commit_pair_multicast(&ctl->tmem_full, kBoth);
+            __syncwarp();
         }
-    mma_done:
-        // all tensor-core work issued by this thread completes before teardown
-        tc_commit_pair_multicast(&ctl->drain, 0x1);
-        mbar_wait(&ctl->drain, 0, ws, nullptr);
+        // all tensor-core work issued by this warp completes before teardown
+        // (elect.sync picks the same lane as above: the commit covers it)
+        if (elect_one()) {
+            tc_commit_pair_multicast(&ctl->drain, 0x1);
+            mbar_wait(&ctl->drain, 0, ws, nullptr);
+        }
+        __syncwarp();
     } else if (warp >= 2 && warp < kFirstScaleWarp) {
         // -------------------------------------------------------- epilogue ----
         const uint32_t q = warp & 3;             // tensor-memory lane quarter of this warp
@@ -596,60 +649,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             epilogue_amax_finish(rmax, tmax, args, ws, gridDim.x * kEpilogueWarps, lane);
         if (lane == 0)
             bulk_wait_all();
-    } else if (warp >= kFirstScaleWarp) {
-        // ----------------------------------------------------- scale warps ----
-        // The one-SM kernel's layout: lane i takes row i (16 bytes) of every
-        // atom of the stage -- this CTA's A rows (steps 0..3), then B's row
-        // tiles 0 and 1 (steps 0..3 each) -- and writes it into its quarter's
-        // lanes: columns slot + 4j for A's step j, slot + 16 + 8j for B's.
-        const uint32_t q = warp & 3;
-        const uint32_t lanes = (q * 32) << 16;
-        const uint32_t ready0 = mapa_shared(smem_u32(&ctl->sf_ready[0]), 0);
-        for (uint32_t i = 0; i < iters; ++i) {
-            const uint32_t s = i % kPStages, u = i % kPSlots;
-            int ok = 1;
-            if (lane == 0) {
-                ok = mbar_wait(&ctl->full[s], (i / kPStages) & 1, ws, abort);
-                // the slot's previous MMAs are done
-                if (ok && i >= kPSlots)
-                    ok = mbar_wait(&ctl->sf_free[u], ((i / kPSlots) - 1) & 1, ws, abort);
-            }
-            if (!__shfl_sync(0xFFFFFFFFu, ok, 0))
-                break;
-            const uint8_t* sfa_s = smem + (size_t)s * kPStage + kPA + kPB + lane * 16;
-            const uint8_t* sfb_s = sfa_s + kSfaBytes;
-            uint32_t v[48];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 a = *reinterpret_cast<const uint4*>(sfa_s + j * 512);
-                const uint4 b0 = *reinterpret_cast<const uint4*>(sfb_s + j * 512);
-                const uint4 b1 = *reinterpret_cast<const uint4*>(sfb_s + (4 + j) * 512);
-                v[4 * j] = a.x;
-                v[4 * j + 1] = a.y;
-                v[4 * j + 2] = a.z;
-                v[4 * j + 3] = a.w;
-                v[16 + 8 * j] = b0.x;
-                v[16 + 8 * j + 1] = b0.y;
-                v[16 + 8 * j + 2] = b0.z;
-                v[16 + 8 * j + 3] = b0.w;
-                v[16 + 8 * j + 4] = b1.x;
-                v[16 + 8 * j + 5] = b1.y;
-                v[16 + 8 * j + 6] = b1.z;
-                v[16 + 8 * j + 7] = b1.w;
-            }
-            const uint32_t col = tmem + lanes + kAccCols + u * kPSlotStride;
-            tmem_st_32x32b_x16(col, v);
-            tmem_st_32x32b_x16(col + 16, v + 16);
-            tmem_st_32x32b_x16(col + 32, v + 32);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive_remote(ready0 + s * (uint32_t)sizeof(uint64_t));
-        }
     }
 
     __syncthreads();
+    // after a failed wait (here or in the peer CTA) tensor copies of this CTA
+    // may still be in flight, their barrier never to complete: give them time
+    // to land before the CTA's shared memory is released
+    if (threadIdx.x == 0 && (*abort || ld_shared_cluster_u32(mapa_shared(smem_u32(&ctl->abort), rank ^ 1u))))
+        __nanosleep(50000);
     // the even CTA's MMAs read this CTA's shared memory and write its tensor
     // memory: neither CTA frees anything before both are done
     cluster_sync_all();
@@ -712,7 +719,7 @@ nvfp4_status launch_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, 
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(kPThreads, 1, 1);
         cfg.dynamicSmemBytes = kPSmemBytes;
         cfg.stream = stream;
         cfg.attrs = attr;
