@@ -345,6 +345,20 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------------- election ----
+// One lane of the converged warp (the lowest active one): the lane that
+// issues asynchronous work (tensor copies, tcgen05 operations, bulk-group
+// commits and waits) on behalf of the warp.  Issued this way from a warp that
+// runs the loop together, such instructions go out at full rate; issued by
+// one lane inside a divergent branch, each tensor-core copy cost ~40-56
+// cycles and the tensor copies of a producer noticeably more latency.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t p;
+    asm volatile("{\n.reg .pred q;\n.reg .b32 r;\nelect.sync r|q, 0xffffffff;\nselp.u32 %0, 1, 0, q;\n}" : "=r"(p));
+    return p != 0;
+}
+
 // ------------------------------------------------------- named barriers ----
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 {

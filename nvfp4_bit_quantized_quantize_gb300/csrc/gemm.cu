@@ -275,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     epilogue_store_bf16(p, row0, c0, args, buf, &tma_d, lane);
             }
         }
-        if (lane == 0)
+        // (the lane that committed the stores: the elected one)
+        if (elect_one())
             bulk_wait_all();
     } else if (warp >= kFirstScaleWarp) {
         // ----------------------------------------------------- scale warps ----
@@ -381,14 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (whose shared and tensor memory the MMAs use) alive until all tensor-core
 // work is done; after a failed wait, every CTA first gives the tensor copies
 // it may have in flight time to land.
-// One lane of the converged warp (the lowest active one).
-__device__ __forceinline__ bool elect_one()
-{
-    uint32_t p;
-    asm volatile("{\n.reg .pred q;\n.reg .b32 r;\nelect.sync r|q, 0xffffffff;\nselp.u32 %0, 1, 0, q;\n}" : "=r"(p));
-    return p != 0;
-}
-
 // One 128 x 4 scale atom (32 rows x 16 bytes of shared memory, every row
 // holding the 4 scales of rows r, r + 32, r + 64, r + 96) into 4 columns of
 // all four lane quarters of tensor memory, in both CTAs of the pair (each
@@ -482,16 +475,25 @@ __global__ void __maxnreg__(128)
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
         // ---------------------------------------------------- TMA producer ----
-        tma_prefetch_desc(&tma_a);
-        tma_prefetch_desc(&tma_b);
-        tma_prefetch_desc(&tma_sfa);
-        tma_prefetch_desc(&tma_sfb);
+        // The whole warp runs the loop: lane 0 waits, one elected lane issues
+        // (a lone lane in a divergent branch issued the copies measurably
+        // slower).
+        if (elect_one()) {
+            tma_prefetch_desc(&tma_a);
+            tma_prefetch_desc(&tma_b);
+            tma_prefetch_desc(&tma_sfa);
+            tma_prefetch_desc(&tma_sfb);
+        }
+        __syncwarp();
         uint32_t ia = 0;  // stages issued
-        for (; ia < iters && !*abort; ++ia) {
+        for (; ia < iters; ++ia) {
             const uint32_t s = ia % kPStages;
-            if (ia >= kPStages && !mbar_wait(&ctl->empty[s], ((ia / kPStages) - 1) & 1, ws, abort))
+            int ok = 1;
+            if (lane == 0)
+                ok = !*abort && (ia < kPStages || mbar_wait(&ctl->empty[s], ((ia / kPStages) - 1) & 1, ws, abort));
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0))
                 break;
             const uint32_t t = cluster + (ia / kstages) * nclusters, ks = ia % kstages;
             const uint32_t tm = t % tiles_m, tn = t / tiles_m;
@@ -502,19 +504,23 @@ __global__ void __maxnreg__(128)
             // CTA for both (a byte count may arrive before the arming: the
             // phase completes only with its one arrival and a zero count)
             const uint32_t bar = mapa_shared(smem_u32(&ctl->full[s]), 0);
-            if (rank == 0)
-                mbar_expect_tx(&ctl->full[s], 2 * kPStage);
-            tma_load_2d_pair(st, &tma_a, bar, (int32_t)(ks * 128), (int32_t)(arow * 128));
-            tma_load_2d_pair(st + kPA, &tma_b, bar, (int32_t)(ks * 128), (int32_t)((2 * tn + rank) * 128));
-            tma_load_3d_pair(st + kPA + kPB, &tma_sfa, bar, 0, (int32_t)(ks * 4), (int32_t)arow);
-            tma_load_3d_pair(st + kPA + kPB + kSfaBytes, &tma_sfb, bar, 0, (int32_t)(ks * 4), (int32_t)(2 * tn));
+            if (elect_one()) {
+                if (rank == 0)
+                    mbar_expect_tx(&ctl->full[s], 2 * kPStage);
+                tma_load_2d_pair(st, &tma_a, bar, (int32_t)(ks * 128), (int32_t)(arow * 128));
+                tma_load_2d_pair(st + kPA, &tma_b, bar, (int32_t)(ks * 128), (int32_t)((2 * tn + rank) * 128));
+                tma_load_3d_pair(st + kPA + kPB, &tma_sfa, bar, 0, (int32_t)(ks * 4), (int32_t)arow);
+                tma_load_3d_pair(st + kPA + kPB + kSfaBytes, &tma_sfb, bar, 0, (int32_t)(ks * 4), (int32_t)(2 * tn));
+            }
+            __syncwarp();
         }
         // never leave with copies in flight: the even CTA's barriers count
         // both CTAs' copies of the stages it armed (after a failed wait the
         // settle below covers the rest)
-        if (rank == 0)
+        if (rank == 0 && lane == 0)
             for (uint32_t k = ia > kPStages ? ia - kPStages : 0; k < ia; ++k)
                 mbar_wait(&ctl->full[k % kPStages], (k / kPStages) & 1, ws, abort);
+        __syncwarp();
     } else if (warp == 1 && rank == 0) {
         // ------------------------------------------------------- MMA warp ----
         const uint32_t base = smem_u32(smem);
@@ -647,7 +653,8 @@ __global__ void __maxnreg__(128)
         // every epilogue warp reports, even one that stopped early
         if (amax_on)
             epilogue_amax_finish(rmax, tmax, args, ws, gridDim.x * kEpilogueWarps, lane);
-        if (lane == 0)
+        // (the lane that committed the stores: the elected one)
+        if (elect_one())
             bulk_wait_all();
     }
 

@@ -52,7 +52,7 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&w)[kN], int base, i
                                             int32_t row0, const GemmArgs& args, uint8_t* buf,
                                             const CUtensorMap* tma_d, int lane)
 {
-    if (lane == 0)
+    if (elect_one())
         bulk_wait_read0();
     __syncwarp();
     uint8_t* row = buf + lane * 32;
@@ -77,7 +77,7 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&w)[kN], int base, i
     }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) {
+    if (elect_one()) {
         tma_store_2d(tma_d, buf, col, row0);
         bulk_commit_group();
     }
@@ -133,7 +133,7 @@ __device__ __forceinline__ void store_wide_chunk(const uint32_t* w, int32_t col,
                                                  const GemmArgs& args, uint8_t* buf, const CUtensorMap* tma_d,
                                                  int lane)
 {
-    if (lane == 0)
+    if (elect_one())
         bulk_wait_read0();
     __syncwarp();
     uint8_t* row = buf + lane * 128;
@@ -162,7 +162,7 @@ __device__ __forceinline__ void store_wide_chunk(const uint32_t* w, int32_t col,
     }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) {
+    if (elect_one()) {
         tma_store_2d(tma_d, buf, col, row0);
         bulk_commit_group();
     }
