@@ -363,12 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 //              CTAs) and issues the MMAs, three copies before each MMA, then
 //              commits the stage free to both CTAs' producers;
 //   warps 2-9  epilogue, as in the one-SM kernel.
-// The copies and MMAs of a stage go out under elect.sync from the converged
-// warp.  Issued by one lane inside a divergent branch, every copy cost the
-// tensor pipe ~40-56 cycles and the whole kernel half its speed; under
-// elect.sync they cost next to nothing.  A stage's scale slot is rewritten
-// only after the stage's next `full`, which the producer armed after the
-// MMAs that read the slot had completed.
+// Every asynchronous instruction goes out from one elected lane of a warp
+// that runs its loop together (lane 0 waits on the barriers): the producer's
+// tensor copies, the MMA warp's scale copies, MMAs and commits, the
+// epilogue's bulk stores.  Issued by one lane inside a divergent branch,
+// every scale copy cost the tensor pipe ~40-56 cycles (the kernel ran at half
+// speed) and the producer's copies went out measurably slower.  A stage's
+// scale slot is rewritten only after the stage's next `full`, which the
+// producer armed after the MMAs that read the slot had completed.
 // Stage-free and accumulator-full signals reach both CTAs through the
 // multicast form of tcgen05.commit; the odd CTA's drained-accumulator signals
 // reach the even CTA by remote mbarrier arrives with the default (CTA-scope
@@ -382,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (whose shared and tensor memory the MMAs use) alive until all tensor-core
 // work is done; after a failed wait, every CTA first gives the tensor copies
 // it may have in flight time to land.
+
 // One 128 x 4 scale atom (32 rows x 16 bytes of shared memory, every row
 // holding the 4 scales of rows r, r + 32, r + 64, r + 96) into 4 columns of
 // all four lane quarters of tensor memory, in both CTAs of the pair (each
