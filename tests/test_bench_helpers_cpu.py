@@ -37,3 +37,21 @@ def test_traffic_reported_only_for_its_source():
     # the hash covers every file the kernel is built from
     h = bench.source_hash(bench.GEMM_SOURCES)
     assert len(h) == 16 and all(os.path.exists(os.path.join(bench.ROOT, f)) for f in bench.GEMM_SOURCES)
+
+
+def test_source_hash_follows_code_not_comments(tmp_path, monkeypatch):
+    # the committed counters stay valid across comment edits and are dropped
+    # by any change of code
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    f = tmp_path / "k.cu"
+    f.write_text("int a = 1;  // one\n\n// note\nint b = 2;\n")
+    h0 = bench.source_hash(["k.cu"])
+    f.write_text("// header\nint a = 1;  // a different comment\nint b = 2;\n\n")
+    assert bench.source_hash(["k.cu"]) == h0
+    f.write_text("int a = 1;\nint b = 3;\n")
+    assert bench.source_hash(["k.cu"]) != h0
+
+
+def test_committed_counters_match_the_current_gemm_code():
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))["nvf4_gemm_pair_kernel"]
+    assert rec["source_hash"] == bench.source_hash(bench.GEMM_SOURCES)
